@@ -1,0 +1,164 @@
+"""Synthetic workload recipes: shapes, lengths, paging and tensor ids.
+
+Nothing here computes any part of the attention method; it only says which
+seeded numbers go where, so that the CUDA library and the oracle see the
+same inputs.
+
+Widths follow the DeepSeek-V2 form of Multi-head Latent Attention as the
+pages give it (liang.world "DeepSeek-V2 architecture revolution", ch. 2:
+d = 5120, n_h = 128, d_h = 128, d_c = 512, d_h^R = 64); the tiny fp32 case
+uses n_h = 4, d_c = 32, d_R = 8, d_h = 16, d = 64.
+
+Recipe (every value is seeded):
+* tensor ids: h=0, W^DKV=1, W^KR=2, W^UK=3, W^UV=4, W_O=5, q=6;
+* h and q ~ N(0, 1); every weight ~ N(0, 1/fan_in), fan_in = input width;
+* sequence b has ``lens[b]`` cached tokens before the step and ``T`` new
+  tokens; h of token p of sequence b is row ``b * row_stride + p`` of a
+  virtual [B * row_stride, d] tensor (row_stride = max(lens) + T);
+* the step appends the T new tokens at positions lens[b] .. lens[b]+T-1
+  and decodes them; query t sits at position lens[b] + t;
+* pages of 64 tokens; each sequence owns ceil((lens[b]+T)/page) pages,
+  taken in order from ``numpy.random.default_rng(1).permutation(num_pages)``
+  when the table is shuffled, else in identity order.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+from . import gen
+
+TID_H, TID_WDKV, TID_WKR, TID_WUK, TID_WUV, TID_WO, TID_Q = range(7)
+
+
+@dataclasses.dataclass(frozen=True)
+class Dims:
+    d_model: int
+    n_heads: int
+    d_nope: int
+    d_v: int
+    d_latent: int
+    d_rope: int
+    page_size: int
+    rope_base: float = 10000.0
+
+    @property
+    def row_width(self) -> int:
+        return self.d_latent + self.d_rope
+
+    @property
+    def softmax_scale(self) -> float:
+        # The pages give no scale; 1/sqrt(d_nope + d_rope) is the stated
+        # assumption (1/sqrt(192) at V2 widths).
+        return 1.0 / math.sqrt(self.d_nope + self.d_rope)
+
+
+V2 = Dims(d_model=5120, n_heads=128, d_nope=128, d_v=128, d_latent=512,
+          d_rope=64, page_size=64)
+TINY = Dims(d_model=64, n_heads=4, d_nope=16, d_v=16, d_latent=32,
+            d_rope=8, page_size=64)
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    dims: Dims
+    dtype: str            # "bf16" or "f32"
+    lens: list            # cached tokens per sequence before the step
+    T: int                # new (query) tokens per sequence
+    shuffle_pages: bool
+    seed: int = 0
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def seq_lens(self) -> list:
+        return [L + self.T for L in self.lens]
+
+    @property
+    def row_stride(self) -> int:
+        return max(self.lens) + self.T
+
+    @property
+    def pages_per_seq(self) -> list:
+        P = self.dims.page_size
+        return [(s + P - 1) // P for s in self.seq_lens]
+
+    @property
+    def max_pages(self) -> int:
+        return max(self.pages_per_seq)
+
+    @property
+    def num_pages(self) -> int:
+        return sum(self.pages_per_seq)
+
+    def block_table(self) -> np.ndarray:
+        """int32 [B, max_pages]; unused entries are -1."""
+        ids = np.arange(self.num_pages, dtype=np.int64)
+        if self.shuffle_pages:
+            ids = np.random.default_rng(1).permutation(self.num_pages)
+        bt = np.full((self.B, self.max_pages), -1, dtype=np.int32)
+        k = 0
+        for b, n in enumerate(self.pages_per_seq):
+            bt[b, :n] = ids[k:k + n]
+            k += n
+        return bt
+
+    # ---- seeded tensors -------------------------------------------------
+    def weight(self, name: str, device="cpu") -> torch.Tensor:
+        d = self.dims
+        spec = {
+            "w_dkv": (TID_WDKV, (d.d_latent, d.d_model), d.d_model),
+            "w_kr": (TID_WKR, (d.d_rope, d.d_model), d.d_model),
+            "w_uk": (TID_WUK, (d.n_heads * d.d_nope, d.d_latent), d.d_latent),
+            "w_uv": (TID_WUV, (d.n_heads * d.d_v, d.d_latent), d.d_latent),
+            "w_o": (TID_WO, (d.d_model, d.n_heads * d.d_v), d.n_heads * d.d_v),
+        }[name]
+        tid, shape, fan_in = spec
+        return gen.fill(self.seed, tid, shape, 1.0 / math.sqrt(fan_in),
+                        self.torch_dtype, device=device)
+
+    def h_rows(self, b: int, p0: int, p1: int, device="cpu") -> torch.Tensor:
+        """Hidden states of tokens p0..p1-1 of sequence b, [p1-p0, d]."""
+        d = self.dims.d_model
+        start = (b * self.row_stride + p0) * d
+        return gen.fill(self.seed, TID_H, (p1 - p0, d), 1.0, self.torch_dtype,
+                        device=device, start=start)
+
+    def q(self, device="cpu") -> torch.Tensor:
+        """Queries [B, T, n_h, d_nope + d_rope] (rope part not rotated)."""
+        d = self.dims
+        return gen.fill(self.seed, TID_Q,
+                        (self.B, self.T, d.n_heads, d.d_nope + d.d_rope), 1.0,
+                        self.torch_dtype, device=device)
+
+
+def c3_lens() -> list:
+    return [int(x) for x in np.random.default_rng(0).integers(1024, 8193, 64)]
+
+
+def config(name: str) -> Workload:
+    """The five named workloads, by the short names used in tests and bench."""
+    if name == "c1":   # tiny fp32 oracle check: 64 cached rows in total
+        return Workload("tiny-fp32-L64", TINY, "f32", [63], 1, False)
+    if name == "c2":   # batch 1, contiguous cache of 4096 tokens
+        return Workload("v2-b1-L4096-contig", V2, "bf16", [4095], 1, False)
+    if name == "c3":   # batch 64, lengths U[1024, 8192], shuffled pages
+        return Workload("v2-b64-paged-Lrand", V2, "bf16", c3_lens(), 1, True)
+    if name == "c4":   # batch 4, 128K cached tokens each
+        return Workload("v2-b4-L131072", V2, "bf16", [131071] * 4, 1, False)
+    if name == "c5":   # batch 128, L=16384, two query tokens, full step
+        return Workload("v2-b128-L16384-T2", V2, "bf16", [16384] * 128, 2, False)
+    raise KeyError(name)
+
+
+CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")

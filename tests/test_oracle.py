@@ -1,0 +1,336 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong scale) fails at least one
+of them; ``test_planted_*`` plant such slips in the oracle and check that
+the pins catch them.
+"""
+import dataclasses
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import brute, mla
+from synth.workloads import TINY, V2, Dims
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _rand_case(dims, S, T, seed):
+    rng = np.random.default_rng(seed)
+    d = dims
+    w = {
+        "w_dkv": rng.standard_normal((d.d_latent, d.d_model)) / math.sqrt(d.d_model),
+        "w_kr": rng.standard_normal((d.d_rope, d.d_model)) / math.sqrt(d.d_model),
+        "w_uk": rng.standard_normal((d.n_heads * d.d_nope, d.d_latent)) / math.sqrt(d.d_latent),
+        "w_uv": rng.standard_normal((d.n_heads * d.d_v, d.d_latent)) / math.sqrt(d.d_latent),
+        "w_o": rng.standard_normal((d.d_model, d.n_heads * d.d_v)) / math.sqrt(d.n_heads * d.d_v),
+    }
+    h = rng.standard_normal((S, d.d_model))
+    q = rng.standard_normal((T, d.n_heads, d.d_nope + d.d_rope))
+    return w, h, q
+
+
+def _rows(dims, w, h):
+    return mla.latent_rows(h, w["w_dkv"], w["w_kr"], np.arange(h.shape[0]), dims.rope_base)
+
+
+def _rel(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-300))
+
+
+SMALL_SHAPES = [
+    Dims(d_model=6, n_heads=1, d_nope=3, d_v=2, d_latent=4, d_rope=2, page_size=4),
+    Dims(d_model=8, n_heads=2, d_nope=4, d_v=3, d_latent=5, d_rope=4, page_size=4),
+    TINY,
+]
+
+
+# --------------------------------------------------------------------------
+# closed forms printed on the pages
+# --------------------------------------------------------------------------
+def test_cache_size_closed_forms():
+    g = _load("cache_sizes.json")
+    assert mla.mha_cache_elems(128, 128) == g["mha_elems_per_token_layer"]
+    assert mla.mla_cache_elems(512, 64) == g["mla_elems_per_token_layer"]
+    assert mla.mla_cache_elems(512, 64, layers=60) == g["mla_elems_60_layers"]
+    assert mla.mha_cache_elems(128, 128, layers=60) == g["mha_elems_60_layers"]
+    assert mla.gqa_equivalent_groups(512, 64, 128) == g["gqa_equivalent_groups"]
+    ratio = mla.mla_cache_elems(512, 64) / mla.mha_cache_elems(128, 128)
+    assert ratio == g["mla_over_mha"]
+    assert mla.mla_cache_elems(512, 64) * 2 == g["bf16_row_bytes"]
+    assert V2.row_width == 576
+    # the quoted 93.3% is vs DeepSeek 67B and does not follow from these widths
+    assert abs((1 - ratio) - g["quoted_reduction_vs_67B_context_only"]) > 0.04
+
+
+# --------------------------------------------------------------------------
+# RoPE
+# --------------------------------------------------------------------------
+def test_rope_golden_pairs():
+    for case in _load("rope_pairs.json")["cases"]:
+        got = mla.rope(np.array(case["x"]), case["pos"], case["base"])
+        np.testing.assert_allclose(got, case["expect"], rtol=0, atol=1e-15)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(3)
+    x, y = rng.standard_normal(64), rng.standard_normal(64)
+    np.testing.assert_array_equal(mla.rope(x, 0), x)
+    for pos in (1, 7, 131071):
+        assert abs(np.linalg.norm(mla.rope(x, pos)) - np.linalg.norm(x)) < 1e-12
+    # <R_m x, R_n y> depends on m - n only
+    a = mla.rope(x, 5) @ mla.rope(y, 3)
+    b = mla.rope(x, 9) @ mla.rope(y, 7)
+    assert abs(a - b) < 1e-12
+    # vectorised positions equal scalar calls
+    X = rng.standard_normal((4, 8))
+    P = np.array([0, 3, 10, 99])
+    np.testing.assert_allclose(mla.rope(X, P), np.stack([mla.rope(X[i], P[i]) for i in range(4)]),
+                               rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# paged addressing
+# --------------------------------------------------------------------------
+def test_slot_of_hand_example_and_bijection():
+    assert mla.slot_of(np.array([[5, 2]]), 0, 6, 4) == 10
+    assert mla.slot_of(np.array([[5, 2]]), 0, 3, 4) == 23
+    rng = np.random.default_rng(0)
+    P, lens = 8, [13, 1, 24, 8]
+    pages = [(L + P - 1) // P for L in lens]
+    perm = rng.permutation(sum(pages))
+    bt = np.full((len(lens), max(pages)), -1)
+    k = 0
+    for b, n in enumerate(pages):
+        bt[b, :n] = perm[k:k + n]
+        k += n
+    slots = [mla.slot_of(bt, b, p, P) for b, L in enumerate(lens) for p in range(L)]
+    assert len(set(slots)) == sum(lens)
+    assert min(slots) >= 0 and max(slots) < sum(pages) * P
+    for b, L in enumerate(lens):
+        for p in range(L):
+            assert mla.slot_of(bt, b, p, P) // P == bt[b, p // P]
+
+
+# --------------------------------------------------------------------------
+# worked examples (hand-derived exact answers)
+# --------------------------------------------------------------------------
+WORKED_DIMS = Dims(d_model=3, n_heads=1, d_nope=1, d_v=1, d_latent=1, d_rope=2, page_size=4)
+
+
+def _worked(case, decode_fn):
+    w = {k: np.array(case[k], dtype=np.float64) for k in ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o")}
+    h = np.array(case["h"])
+    rows = _rows(WORKED_DIMS, w, h)
+    q = np.array(case["q"]).reshape(1, 1, 3)
+    return decode_fn(WORKED_DIMS, rows, q, w, 1)["u"][0]
+
+
+@pytest.mark.parametrize("form", ["explicit", "absorbed"])
+def test_worked_examples(form):
+    fn = mla.decode_explicit if form == "explicit" else mla.decode_absorbed
+    for case in _load("worked_examples.json")["cases"]:
+        np.testing.assert_allclose(_worked(case, fn), case["expect_u"], rtol=0, atol=1e-14,
+                                   err_msg=case["name"])
+
+
+def test_worked_examples_brute():
+    for case in _load("worked_examples.json")["cases"]:
+        w = {k: case[k] for k in ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o")}
+        u = brute.decode(WORKED_DIMS, case["h"], [[case["q"][0]]], w, 1)[0]
+        np.testing.assert_allclose(u, case["expect_u"], rtol=0, atol=1e-14, err_msg=case["name"])
+
+
+# --------------------------------------------------------------------------
+# brute force vs vectorised explicit; absorbed vs explicit
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dims", SMALL_SHAPES)
+@pytest.mark.parametrize("S,T", [(1, 1), (5, 1), (5, 2), (64, 1)])
+def test_brute_force_agrees(dims, S, T):
+    if dims is TINY and S != 64 and T == 1:
+        pytest.skip("tiny widths run at S=64 and the T=2 case only")
+    w, h, q = _rand_case(dims, S, T, seed=S * 10 + T)
+    ref = mla.decode_explicit(dims, _rows(dims, w, h), q, w, T)["u"]
+    bw = {k: v.tolist() for k, v in w.items()}
+    got = np.array(brute.decode(dims, h.tolist(), q.tolist(), bw, T))
+    assert _rel(got, ref) < 1e-12
+
+
+@pytest.mark.parametrize("dims", SMALL_SHAPES + [
+    dataclasses.replace(V2, d_model=256, n_heads=4)])
+@pytest.mark.parametrize("S,T", [(1, 1), (70, 1), (70, 2)])
+def test_absorbed_equals_explicit(dims, S, T):
+    w, h, q = _rand_case(dims, S, T, seed=S + T)
+    rows = _rows(dims, w, h)
+    e = mla.decode_explicit(dims, rows, q, w, T)
+    a = mla.decode_absorbed(dims, rows, q, w, T)
+    assert _rel(a["u"], e["u"]) < 1e-12
+    assert _rel(a["o"], e["o"]) < 1e-12
+    # latent output and value recovery: o_i = W^UV_i o_lat_i
+    w_uv = w["w_uv"].reshape(dims.n_heads, dims.d_v, dims.d_latent)
+    assert _rel(np.einsum("hvc,thc->thv", w_uv, a["o_lat"]), e["o"]) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# softmax and masking invariants, special cases
+# --------------------------------------------------------------------------
+def test_softmax_rows_and_causal_mask():
+    dims = TINY
+    w, h, q = _rand_case(dims, 40, 2, seed=1)
+    rows = _rows(dims, w, h)
+    a = mla.decode_explicit(dims, rows, q, w, 2, return_attn=True)["attn"]
+    assert (a >= 0).all()
+    np.testing.assert_allclose(a.sum(-1), 1.0, rtol=0, atol=1e-12)
+    assert (a[0, :, 39] == 0).all()          # token at 38 does not see 39
+    assert (a[1, :, 39] > 0).all()
+    for t in range(2):
+        for hd in range(dims.n_heads):
+            np.testing.assert_allclose(
+                mla.attention_weights_absorbed(dims, rows, q, w, 2, t, hd),
+                a[t, hd, :38 + t + 1], rtol=0, atol=1e-12)
+
+
+def test_single_slot_ignores_query():
+    dims = TINY
+    w, h, q = _rand_case(dims, 1, 1, seed=2)
+    rows = _rows(dims, w, h)
+    u1 = mla.decode_explicit(dims, rows, q, w, 1)["u"]
+    u2 = mla.decode_explicit(dims, rows, 3.0 * q + 1.0, w, 1)["u"]
+    c0 = rows[0, :dims.d_latent]
+    expect = w["w_o"] @ (w["w_uv"] @ c0)      # a = [1]: o_i = W^UV_i c_0
+    assert _rel(u1[0], expect) < 1e-12 and _rel(u2[0], expect) < 1e-12
+
+
+def test_equal_rows_give_single_slot_answer():
+    dims = TINY
+    w, h, q = _rand_case(dims, 1, 1, seed=4)
+    rows = np.repeat(_rows(dims, w, h), 17, axis=0)
+    u = mla.decode_absorbed(dims, rows, q, w, 1)["u"]
+    expect = w["w_o"] @ (w["w_uv"] @ rows[0, :dims.d_latent])
+    assert _rel(u[0], expect) < 1e-12
+
+
+def test_zero_query_and_rope_key_is_uniform():
+    dims = TINY
+    w, h, q = _rand_case(dims, 33, 1, seed=5)
+    w["w_kr"] = np.zeros_like(w["w_kr"])
+    q = np.zeros_like(q)
+    rows = _rows(dims, w, h)
+    o = mla.decode_explicit(dims, rows, q, w, 1)["o"][0]
+    c_mean = rows[:, :dims.d_latent].mean(axis=0)
+    expect = (w["w_uv"] @ c_mean).reshape(dims.n_heads, dims.d_v)
+    assert _rel(o, expect) < 1e-12
+
+
+def test_two_tokens_equal_two_single_decodes():
+    dims = TINY
+    w, h, q = _rand_case(dims, 30, 2, seed=6)
+    rows = _rows(dims, w, h)
+    both = mla.decode_explicit(dims, rows, q, w, 2)["u"]
+    first = mla.decode_explicit(dims, rows[:29], q[:1], w, 1)["u"]
+    second = mla.decode_explicit(dims, rows, q[1:], w, 1)["u"]
+    assert _rel(both[0], first[0]) < 1e-13 and _rel(both[1], second[0]) < 1e-13
+
+
+def test_rope_key_is_shared_and_in_row():
+    """k^R occupies columns d_c.. of the row, is the same for every head and
+    carries the position (caching only c^KV would lose it)."""
+    dims = TINY
+    w, h, _ = _rand_case(dims, 3, 1, seed=7)
+    rows = _rows(dims, w, h)
+    np.testing.assert_allclose(rows[:, :dims.d_latent], h @ w["w_dkv"].T, rtol=0, atol=1e-13)
+    raw = h @ w["w_kr"].T
+    for p in range(3):
+        np.testing.assert_allclose(rows[p, dims.d_latent:], mla.rope(raw[p], p), rtol=0, atol=1e-13)
+    moved = mla.latent_rows(h, w["w_dkv"], w["w_kr"], np.arange(3) + 5)
+    assert np.abs(moved[:, dims.d_latent:] - rows[:, dims.d_latent:]).max() > 1e-3
+
+
+def test_error_stats():
+    s = mla.error_stats(np.array([1.0, -2.0, 2.5]), np.array([1.0, -2.0, 3.0]))
+    assert s["max_rel"] == pytest.approx(0.5 / 3.0) and s["mean_rel"] == pytest.approx(0.5 / 6.0)
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each must be caught by one of the pins above
+# --------------------------------------------------------------------------
+def _pins_pass():
+    try:
+        test_rope_golden_pairs()
+        for form in ("explicit", "absorbed"):
+            test_worked_examples(form)
+        test_brute_force_agrees(SMALL_SHAPES[1], 5, 2)
+        test_absorbed_equals_explicit(SMALL_SHAPES[1], 70, 2)
+        test_softmax_rows_and_causal_mask()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_planted_rope_sign(monkeypatch):
+    orig = mla.rope
+    monkeypatch.setattr(mla, "rope", lambda x, pos, base=10000.0: orig(x, -np.asarray(pos), base))
+    assert not _pins_pass()
+
+
+def test_planted_rope_frequency(monkeypatch):
+    orig = mla.rope
+    monkeypatch.setattr(mla, "rope", lambda x, pos, base=10000.0: orig(x, pos, base * 2))
+    assert not _pins_pass()
+
+
+def test_planted_scale(monkeypatch):
+    monkeypatch.setattr(Dims, "softmax_scale", property(lambda s: 1.0 / math.sqrt(s.d_nope)))
+    assert not _pins_pass()
+
+
+def test_planted_head_slicing(monkeypatch):
+    orig = mla.decode_explicit
+
+    def bad(dims, rows, q, w, T, return_attn=False):
+        w2 = dict(w)
+        H, dn = dims.n_heads, dims.d_nope
+        w2["w_uk"] = np.asarray(w["w_uk"]).reshape(dn, H, -1).transpose(1, 0, 2).reshape(H * dn, -1)
+        return orig(dims, rows, q, w2, T, return_attn)
+    monkeypatch.setattr(mla, "decode_explicit", bad)
+    assert not _pins_pass()
+
+
+def test_planted_dropped_rope_key(monkeypatch):
+    orig = mla.latent_rows
+
+    def bad(h, w_dkv, w_kr, positions, base=10000.0):
+        r = orig(h, w_dkv, w_kr, positions, base)
+        r[:, np.asarray(w_dkv).shape[0]:] = 0.0
+        return r
+    monkeypatch.setattr(mla, "latent_rows", bad)
+    assert not _pins_pass()
+
+
+def test_planted_unmasked_future(monkeypatch):
+    orig = mla.decode_explicit
+
+    def bad(dims, rows, q, w, T, return_attn=False):
+        # every query sees every row (drops the causal mask between new tokens)
+        out = {"u": [], "o": []}
+        for t in range(T):
+            r = orig(dims, rows, q[t:t + 1], w, 1, return_attn)
+            out["u"].append(r["u"][0])
+            out["o"].append(r["o"][0])
+        res = {k: np.stack(v) for k, v in out.items()}
+        if return_attn:
+            res["attn"] = np.stack([orig(dims, rows, q[t:t + 1], w, 1, True)["attn"][0]
+                                    for t in range(T)])
+        return res
+    monkeypatch.setattr(mla, "decode_explicit", bad)
+    assert not _pins_pass()
