@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""MLA decode benchmark on B300: prints one JSON line.
+
+One step = one pass of the whole hot path over the workload's batch:
+compress + RoPE + paged append of the T new tokens of every sequence, then
+the absorbed decode (query absorption, split-KV attention, combine + W^UV,
+W_O).  Inputs and state are resident in HBM when the timed region starts;
+L2 is flushed (a 2x-L2 buffer is written) before every timed step, outside
+the step's own CUDA-event bracket.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
+                  [--impl mla|reference]
+
+--impl reference times the fp64 CPU oracle (the reference of this build)
+on the same workload, a bounded sample per step.  Under torchrun (N > 1)
+every rank runs an independent replica on its own GPU (the step has no
+cross-GPU exchange); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s and latent-cache GB/s (% of B300 roofline), 1 GPU"
+DEFAULT_STEPS = {"c1": 200, "c2": 1000, "c3": 300, "c4": 300, "c5": 50}
+
+
+# ----------------------------------------------------------------------------- setup
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    a = ap.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.config]
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- work model
+def work_model(wl):
+    """Algorithmic bytes and FLOPs per launch of each kernel, and per step."""
+    d = wl.dims
+    es = 2 if wl.dtype == "bf16" else 4
+    M, H, dc, dr, R = wl.B * wl.T, d.n_heads, d.d_latent, d.d_rope, d.row_width
+    dn, dv, D = d.d_nope, d.d_v, d.d_model
+    cache_rows = sum(wl.seq_lens)
+    visible = sum(S - wl.T + t + 1 for S in wl.seq_lens for t in range(wl.T))
+    k = {
+        "compress_append": (R * D * es + M * D * es + M * R * es, 2.0 * M * R * D),
+        "absorb_q": (H * dn * dc * es + M * H * (dn + dr) * es + M * H * R * es,
+                     2.0 * M * H * dn * dc),
+        "attend": (cache_rows * R * es + M * H * R * es, 2.0 * visible * H * (R + dc)),
+        "combine_uv": (H * dv * dc * es + M * H * dv * es, 2.0 * M * H * dv * dc),
+        "out_proj": (D * H * dv * es + M * H * dv * es + M * D * es, 2.0 * M * D * H * dv),
+        "plan": (wl.B * 4, 0.0),
+    }
+    tot_bytes = (R * D + H * dn * dc + H * dv * dc + D * H * dv) * es \
+        + cache_rows * R * es + M * (D + H * (dn + dr) + D) * es
+    tot_flops = sum(f for _, f in k.values())
+    return k, tot_bytes, tot_flops, cache_rows * R * es
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, bus_id):
+        self.samples = []
+        self.proc = None
+        self.bus_id = bus_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.bus_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "during the timed region"
+        if not win:
+            win = [s for s in self.samples if t0 - 1.0 <= s[0] <= t1 + 1.0]
+            note = "within 1 s of the timed region (region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        sm = sorted(v for v in (num(p[0]) for _, p in win) if v is not None)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in win:
+            for n, v in zip(names, p[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": num(win[0][1][1]),
+                "power_w_max": max((num(p[2]) or 0.0) for _, p in win),
+                "reasons": sorted(reasons), "samples": len(win), "note": note}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample_setup(wl, device):
+    """fp64 state for timing the oracle on one sequence (b = 0), untimed."""
+    import numpy as np
+    import torch
+    from oracle import case as ocase
+    from oracle import mla as omla
+    w64 = ocase.weights_f64(wl, device=device)
+    L = wl.lens[0]
+    rows = np.empty((L, wl.dims.row_width))
+    for p0 in range(0, L, 8192):
+        p1 = min(L, p0 + 8192)
+        h = wl.h_rows(0, p0, p1, device=device).to(torch.float64).cpu().numpy()
+        rows[p0:p1] = omla.latent_rows(h, w64["w_dkv"], w64["w_kr"], np.arange(p0, p1),
+                                       wl.dims.rope_base)
+    h_new = wl.h_rows(0, L, L + wl.T, device=device).to(torch.float64).cpu().numpy()
+    q64 = wl.q(device=device)[0].to(torch.float64).cpu().numpy()
+    return {"w": w64, "rows": rows, "h_new": h_new, "q": q64}
+
+
+def oracle_sample_step(wl, st, head):
+    """One oracle decode step of sequence 0 restricted to one head.
+
+    The unmodified oracle functions run on the head's slices of W^UK, W^UV
+    and W_O (its contribution to u); the new tokens' rows are appended first.
+    """
+    import numpy as np
+    from oracle import mla as omla
+    d = wl.dims
+    L = wl.lens[0]
+    new = omla.latent_rows(st["h_new"], st["w"]["w_dkv"], st["w"]["w_kr"],
+                           np.arange(L, L + wl.T), d.rope_base)
+    rows = np.concatenate([st["rows"], new])
+    w = {"w_uk": st["w"]["w_uk"][head * d.d_nope:(head + 1) * d.d_nope],
+         "w_uv": st["w"]["w_uv"][head * d.d_v:(head + 1) * d.d_v],
+         "w_o": st["w"]["w_o"][:, head * d.d_v:(head + 1) * d.d_v]}
+    one = dataclasses.replace(d, n_heads=1)
+    return omla.decode_explicit(one, rows, st["q"][:, head:head + 1], w, wl.T)["u"]
+
+
+def time_oracle(wl, st, steps=None, seconds=None):
+    """Returns (tokens/s, seconds timed, steps timed, sample description)."""
+    H = wl.dims.n_heads
+    per_step_tokens = wl.T / H        # one head of one sequence's T tokens
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_sample_step(wl, st, n % H)
+        n += 1
+        el = time.perf_counter() - t0
+        if steps is not None and n >= steps:
+            break
+        if seconds is not None and el >= seconds:
+            break
+    sample = (f"sequence 0 (cache {wl.lens[0]} + {wl.T} new tokens), one of {H} heads per step, "
+              f"explicit fp64 form incl. the new rows' W^DKV/W^KR; tokens/s = T/{H} per step "
+              f"/ step time")
+    return per_step_tokens * n / el, el, n, sample
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(a, wl, rank, world):
+    if rank != 0:
+        return None
+    st = oracle_sample_setup(wl, "cpu" if not _cuda() else "cuda:0")
+    for _ in range(a.warmup):
+        oracle_sample_step(wl, st, 0)
+    tps, el, n, sample = time_oracle(wl, st, steps=a.steps)
+    return {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": 1e3 * el / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "batch": wl.B, "T": wl.T},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def _cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+def run_mla(a, wl, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+    import mla_latent_kv_82_b300 as m
+    from mla_latent_kv_82_b300.workload import DeviceState
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    st = DeviceState(wl, device=local_rank)
+    torch.cuda.synchronize()
+    l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        st.step()
+    torch.cuda.synchronize()
+    if st.mla.check_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0" \
+        if hasattr(props, "pci_bus_id") else str(local_rank)
+    clocks = ClockSampler(bus)
+    clocks.start()
+    time.sleep(0.3)
+
+    m.mla_profile_enable(st.mla.ctx, 1)
+    kt = {}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    launches0 = st.mla.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(a.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        st.step()
+        evs[i][1].record(stream)
+        for name, ms in m.mla_profile_read(st.mla.ctx):
+            kt.setdefault(name, []).append(ms)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    launches = st.mla.launch_count() - launches0
+    m.mla_profile_enable(st.mla.ctx, 0)
+    step_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    if world > 1:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    status = st.mla.check_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    time.sleep(0.2)
+    clocks.stop()
+
+    tokens = wl.B * wl.T * a.steps * world
+    value = tokens / (step_ms * 1e-3)
+    ms_per_step = step_ms / a.steps
+
+    # ---- roofline of the dominant kernel and of the whole step
+    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl)
+    avg = {k: sum(v) / len(v) for k, v in kt.items() if v}
+    share = {k: sum(v) for k, v in kt.items()}
+    dom = max(share, key=share.get)
+    b_dom, f_dom = kmodel[dom]
+    t_dom = avg[dom] * 1e-3
+    bw_peak = peaks["hbm_gbs"]
+    tf_peak = peaks["bf16_tflops"]
+    mem_bound = (b_dom / (bw_peak * 1e9)) >= (f_dom / (tf_peak * 1e12)) or wl.dtype != "bf16"
+    if mem_bound:
+        roof = {"bound": "hbm", "achieved": b_dom / t_dom / 1e9, "peak": bw_peak,
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": f_dom / t_dom / 1e12, "peak": tf_peak,
+                "unit": "TFLOP/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": dom,
+                 "traffic": None, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 if peaks["source"] == "measured" else "fallback",
+                 "algorithmic_bytes_per_launch": b_dom, "algorithmic_flops_per_launch": f_dom,
+                 "avg_launch_ms": avg[dom]})
+    t_step = ms_per_step * 1e-3
+    step_roof = max(tot_bytes / (bw_peak * 1e9), tot_flops / (tf_peak * 1e12))
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if not a.no_e2e:
+        h_h = st.h_new.cpu().pin_memory()
+        q_h = st.q.cpu().pin_memory()
+        p_h = st.pos_new.cpu().pin_memory()
+        s_h = st.seq_lens.cpu().pin_memory()
+        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        e_steps = min(a.steps, 200)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e_steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(e_steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            st.h_new.copy_(h_h, non_blocking=True)
+            st.q.copy_(q_h, non_blocking=True)
+            st.pos_new.copy_(p_h, non_blocking=True)
+            st.seq_lens.copy_(s_h, non_blocking=True)
+            st.step()
+            out_h.copy_(st.out, non_blocking=True)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": wl.B * wl.T * e_steps * world / (e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (h_h, q_h, p_h, s_h)),
+               "d2h_bytes_per_step": out_h.numel() * out_h.element_size(), "steps": e_steps,
+               "note": "inputs copied from pinned host memory and the output copied back "
+                       "inside the timed region of every step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        ost = oracle_sample_setup(wl, f"cuda:{local_rank}")
+        tps, el, n, sample = time_oracle(wl, ost, seconds=a.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample + f"; {n} steps in {el:.1f} s"}
+
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded N(0,1) hidden states and queries, N(0,1/fan_in) weights",
+        "config": {"workload": wl.name, "batch": wl.B, "T": wl.T,
+                   "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
+                   f"({2 * l2 >> 20} MiB write, outside the step's event bracket)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "cache_gbs": cache_bytes / t_step / 1e9,
+                   "step_algorithmic_gb": tot_bytes / 1e9,
+                   "step_algorithmic_gflop": tot_flops / 1e9,
+                   "step_roofline_frac": step_roof / t_step,
+                   "kernel_ms": {k: round(v, 5) for k, v in avg.items()},
+                   "kernel_share": {k: round(v / sum(share.values()), 4) for k, v in share.items()}},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+
+
+def main():
+    a = parse()
+    rank, local_rank, world = dist_info()
+    from synth import workloads as W
+    wl = W.config(a.config)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if a.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        res = run_reference(a, wl, rank, world) if a.impl == "reference" \
+            else run_mla(a, wl, rank, local_rank, world)
+    finally:
+        if world > 1 and a.impl != "reference":
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * mla.h -- C ABI of a single-GPU Multi-head Latent Attention (MLA) decode
+ * library for NVIDIA B300 (sm_103a).
+ *
+ * What the library computes is the DeepSeek-V2 form of MLA as stated on the
+ * page "DeepSeek-V2：在“大力出奇迹”的AI军备竞赛中，四两拨千斤" (liang.world),
+ * 第二章 "侠客甲——MLA" §1-§3, and restated on "DeepSeek 系列模型技术深度解读"
+ * (tuntang.top), section "Multi-head Latent Attention (MLA)":
+ *
+ *   per token:  c^KV = W^DKV h,  k^R = RoPE_pos(W^KR h)          (cached)
+ *   per query:  q_i = [q^C_i ; RoPE_pos(q^R_i)],
+ *               k_{p,i} = [W^UK_i c_p ; k^R_p],  v_{p,i} = W^UV_i c_p,
+ *               o_i = softmax_p(q_i . k_{p,i} * scale) . v_{.,i},
+ *               u = W_O [o_1; ...; o_{n_h}].
+ *
+ * Only the 576-wide row [c^KV ; k^R] is cached per token (bf16: 1152 bytes).
+ * Decode never forms K or V: W^UK is folded into the query and W^UV is
+ * applied to the attention output (the absorption paragraph of §2).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are CUDA device pointers on the context's
+ *    device; the caller owns them and keeps them alive until the work that
+ *    uses them has finished on the stream.  The context borrows the weight
+ *    pointers from mla_create until mla_destroy.
+ *  - All matrices are row-major.  Matrices act on column vectors ("W h"):
+ *      w_dkv [d_latent, d_model]          w_kr [d_rope, d_model]
+ *      w_uk  [n_heads*d_nope, d_latent]   w_uv [n_heads*d_v, d_latent]
+ *      w_o   [d_model, n_heads*d_v]
+ *    Head i owns rows i*d_nope.. of w_uk and i*d_v.. of w_uv.
+ *  - Element type of every float buffer is the context dtype (bf16 or
+ *    fp32).  Index buffers are int32.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and never synchronise, except mla_check_status.
+ *  - Argument errors are returned before anything is enqueued.  Errors found
+ *    on the device (a page id or length out of range, a bounded wait that
+ *    gave up) set a status word on the device; the offending access is
+ *    skipped and mla_check_status reports the error.  No call traps,
+ *    asserts or exits.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer  */
+  MLA_ERR_UNSUPPORTED = 2,   /* widths or device this build does not serve */
+  MLA_ERR_CUDA = 3,          /* a CUDA runtime call failed                 */
+  MLA_ERR_WORKSPACE = 4,     /* workspace smaller than mla_decode_workspace_size */
+  MLA_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up         */
+  MLA_ERR_DEVICE_INDEX = 6   /* device saw a page id / length out of range */
+} mla_status;
+
+typedef enum { MLA_BF16 = 0, MLA_FP32 = 1 } mla_dtype;
+
+/* Model widths.  bf16 contexts run the tensor-core kernels and need the
+ * DeepSeek-V2 head widths: n_heads 128, d_nope 128, d_v 128, d_latent 512,
+ * d_rope 64, page_size 64, and d_model a multiple of 64 (<= 16384).
+ * fp32 contexts run plain fp32 kernels for small widths: n_heads <= 128,
+ * d_latent <= 512, d_latent + d_rope <= 576, d_rope even, d_nope, d_v
+ * <= 512, any page_size >= 1.  softmax_scale is applied to q.k; the pages
+ * give none (1/sqrt(d_nope + d_rope) is the usual choice).  rope_base is
+ * the RoPE frequency base; positions must stay below max_position. */
+typedef struct {
+  int d_model;
+  int n_heads;
+  int d_nope;
+  int d_v;
+  int d_latent;
+  int d_rope;
+  int page_size;
+  int max_position;
+  float softmax_scale;
+  float rope_base;
+  mla_dtype dtype;
+} mla_config;
+
+/* Device pointers to the five projection matrices (layouts above). */
+typedef struct {
+  const void* w_dkv;
+  const void* w_kr;
+  const void* w_uk;
+  const void* w_uv;
+  const void* w_o;
+} mla_weights;
+
+typedef struct mla_ctx mla_ctx;
+
+/* Create a context on CUDA device `device`: validates the widths, builds
+ * the RoPE cos/sin table (float64 on the host, stored as fp32 on the
+ * device, [max_position, d_rope/2]) and allocates the device status word.
+ * The weights are borrowed, not copied.  On success *out owns those two
+ * allocations until mla_destroy. */
+mla_status mla_create(const mla_config* cfg, const mla_weights* weights,
+                      int device, mla_ctx** out);
+
+/* Free what mla_create allocated.  Synchronises the device first. */
+mla_status mla_destroy(mla_ctx* ctx);
+
+/* Compress + RoPE + paged append (liang.world ch.2 §2, §3; the RoPE key is
+ * cached with the latent, www.pptc.cn/news/140720 §3.4).
+ *   h           device, [batch*T, d_model]; row b*T+t is token t of
+ *               sequence b.
+ *   positions   device int32 [batch*T]: position of each token (0-based,
+ *               < max_position).
+ *   block_table device int32 [batch, max_pages]: physical page of each
+ *               logical page of each sequence.
+ *   cache       device, [num_pages*page_size, d_latent+d_rope], the pool.
+ * Writes row [W^DKV h ; RoPE_pos(W^KR h)] (fp32 accumulation, rounded once
+ * to the context dtype) to pool row
+ *   block_table[b][pos / page_size] * page_size + pos % page_size.
+ * Rows of other tokens are untouched.  A page id outside [0, num_pages) or
+ * a position out of range skips that token and sets MLA_ERR_DEVICE_INDEX.
+ * Any batch*T >= 1 is accepted (prefill chunks included). */
+mla_status mla_compress_append(mla_ctx* ctx, const void* h, int batch, int T,
+                               const int32_t* positions,
+                               const int32_t* block_table, int max_pages,
+                               void* cache, int num_pages, void* stream);
+
+/* Bytes of scratch memory mla_decode needs for this batch shape. */
+size_t mla_decode_workspace_size(const mla_ctx* ctx, int batch, int T,
+                                 int max_pages);
+
+/* Absorbed decode of the last T tokens of each sequence (liang.world ch.2
+ * §1-§3; absorption of W^UK into the query and of W^UV after attention).
+ *   q          device, [batch, T, n_heads, d_nope + d_rope]: q^C then the
+ *              un-rotated q^R of each head.
+ *   cache      device pool as written by mla_compress_append (the T query
+ *              tokens must already be appended).
+ *   seq_lens   device int32 [batch]: cached tokens per sequence, the query
+ *              tokens included.  Query t of sequence b sits at position
+ *              seq_lens[b] - T + t and attends to positions 0..itself.
+ *   out        device, [batch, T, d_model]: u = W_O [o_1 ... o_{n_h}].
+ *   workspace  device scratch of at least mla_decode_workspace_size bytes,
+ *              256-byte aligned; its contents need not be initialised.
+ * A length outside [T, max_pages*page_size] or a bad page id sets
+ * MLA_ERR_DEVICE_INDEX on the device; the bad part is skipped. */
+mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache,
+                      int num_pages, const int32_t* block_table, int max_pages,
+                      const int32_t* seq_lens, int batch, int T, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Offsets (bytes from the workspace start) of two intermediates that
+ * mla_decode leaves in the workspace, for diagnostics: the latent attention
+ * output o_lat [batch*T, n_heads, d_latent] (sum_p a_p c_p) and the value
+ * output o [batch*T, n_heads*d_v], both in the context dtype. */
+mla_status mla_decode_workspace_offsets(const mla_ctx* ctx, int batch, int T,
+                                        int max_pages, size_t* o_lat_offset,
+                                        size_t* o_offset);
+
+/* Synchronise `stream`, then read and clear the device status word.
+ * Returns MLA_OK, MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_INDEX or MLA_ERR_CUDA. */
+mla_status mla_check_status(mla_ctx* ctx, void* stream);
+
+/* Number of kernels this context has enqueued since creation. */
+int64_t mla_launch_count(const mla_ctx* ctx);
+
+/* Diagnostic: enqueue one kernel whose single bounded wait on an mbarrier
+ * that nothing arrives on gives up after about `spin_limit` polls and
+ * records MLA_ERR_TIMEOUT in the status word (the path every in-kernel wait
+ * of this library takes when it gives up). */
+mla_status mla_selftest_bounded_wait(mla_ctx* ctx, int spin_limit, void* stream);
+
+/* Per-kernel timing for benchmarks.  While enabled, every call records a
+ * CUDA event on its stream before each kernel it enqueues and one after the
+ * last; mla_profile_read waits for the recorded events and writes, for at
+ * most `max_kernels` kernels enqueued since the previous read, the kernel's
+ * name (a static string) and its duration in milliseconds.  It returns the
+ * number written (or -1 on error) and forgets the recorded events.  At most
+ * 64 events are kept between reads; later kernels are not recorded. */
+mla_status mla_profile_enable(mla_ctx* ctx, int enable);
+int mla_profile_read(mla_ctx* ctx, float* ms, const char** names, int max_kernels);
+
+/* Static string naming a status code. */
+const char* mla_status_string(mla_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

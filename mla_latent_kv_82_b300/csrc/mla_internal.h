@@ -1,0 +1,73 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "mla.h"
+
+// Status word layout on the device: [code, detail, count, spare].
+enum { MLA_ST_CODE = 0, MLA_ST_DETAIL = 1, MLA_ST_COUNT = 2, MLA_ST_WORDS = 4 };
+
+struct mla_ctx {
+  mla_config cfg;
+  mla_weights w;
+  int device;
+  int num_sms;
+  float2* rope_cs;     // device [max_position, d_rope/2] of (cos, sin)
+  int* status;         // device [MLA_ST_WORDS]
+  int64_t launches;
+  // per-kernel timing (mla_profile_enable)
+  bool prof = false;
+  int n_marks = 0;
+  cudaEvent_t marks[64];
+  const char* mark_names[64];
+};
+
+namespace mla {
+
+// Byte layout of the decode workspace (all offsets 256-byte aligned).
+struct WsLayout {
+  int G;           // KV splits of the global page list
+  int n_slots;     // partial-result slots (G + batch bounds the segment count)
+  size_t lens, page_prefix, first_split, slot_base;   // int32 arrays
+  size_t meta;     // int32 [4]: splits in use G_eff = min(G, pages), total pages
+  size_t qfull;    // [batch*T, n_heads, R] query rows in the dtype (image layout for bf16)
+  size_t part_o;   // fp32 [n_slots, T, n_heads, d_latent]
+  size_t part_lse; // fp32 [n_slots, T, n_heads] (log2 domain)
+  size_t o_lat;    // dtype [batch*T, n_heads, d_latent]
+  size_t o;        // dtype [batch*T, n_heads*d_v]
+  size_t total;
+};
+
+// Record a timing mark on `st` when profiling is on: `name` is the kernel
+// enqueued next, nullptr closes the previous one.
+void prof_mark(mla_ctx* ctx, cudaStream_t st, const char* name);
+
+WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages);
+
+// Splits the global page list across G workers; see plan.cu.
+void launch_plan(const mla_ctx* ctx, const WsLayout& L, char* ws, const int32_t* seq_lens,
+                 int B, int T, int max_pages, cudaStream_t st);
+
+// fp32 kernels (any small widths).
+void f32_compress_append(mla_ctx* ctx, const float* h, int B, int T, const int32_t* pos,
+                         const int32_t* bt, int max_pages, float* cache, int num_pages,
+                         cudaStream_t st);
+void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,
+                const int32_t* bt, int max_pages, int B, int T, float* out, char* ws,
+                const WsLayout& L, cudaStream_t st);
+
+// bf16 kernels (DeepSeek-V2 head widths).
+void bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
+                          const int32_t* pos, const int32_t* bt, int max_pages,
+                          __nv_bfloat16* cache, int num_pages, cudaStream_t st);
+void bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+                 int num_pages, const int32_t* bt, int max_pages, int B, int T,
+                 __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
+
+void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
+
+}  // namespace mla

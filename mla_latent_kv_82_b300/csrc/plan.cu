@@ -1,0 +1,184 @@
+// Split-KV work plan and workspace layout.
+//
+// Long caches are split across SMs (flash-decoding style) and merged with a
+// log-sum-exp combine.  The plan is built on the device from seq_lens so the
+// host never waits for it:
+//   * pages(b)      = ceil(len_b / page_size), len_b validated and clamped;
+//   * prefix[b]     = pages of sequences 0..b-1  (prefix[B] = P, all pages);
+//   * G_eff = min(G, P) splits are used, so none is empty; split c < G_eff
+//     owns global pages [floor(cP/G_eff), floor((c+1)P/G_eff));
+//   * first_split[b] = split holding page prefix[b]; the splits touching
+//     sequence b are first_split[b] .. split(prefix[b+1]-1);
+//   * slot_base[b]   = partial-result slots of sequences 0..b-1; split c's
+//     piece of sequence b lands in slot slot_base[b] + c - first_split[b].
+// Every split does the same number of pages (+-1), whatever the length mix.
+#include "device_util.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ long long split_of_page(long long g, long long P, int G) {
+  return ((g + 1) * G - 1) / P;
+}
+
+// Block-wide exclusive scan of one int per thread; returns the block total.
+__device__ int block_exclusive_scan(int v, int* out, int* tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = (lane < (int)(blockDim.x >> 5)) ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    tmp[lane] = s;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int total = tmp[(blockDim.x >> 5) - 1];
+  *out = x - v + (warp > 0 ? tmp[warp - 1] : 0);
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int page, int max_pages,
+            int max_position, int G_max, int* lens, int* prefix, int* first_split,
+            int* slot_base, int* meta, int* status) {
+  __shared__ int tmp[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  // pass 1: validated lengths and the page prefix
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int b = base + threadIdx.x;
+    int pages = 0;
+    if (b < B) {
+      int len = seq_lens[b];
+      const int cap = min(max_pages * page, max_position);
+      if (len < T || len > cap) {
+        report(status, MLA_ERR_DEVICE_INDEX, 1000000 + b);
+        len = len < T ? T : cap;
+      }
+      lens[b] = len;
+      pages = (len + page - 1) / page;
+    }
+    int ex;
+    const int tot = block_exclusive_scan(pages, &ex, tmp);
+    if (b < B) prefix[b] = carry + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    prefix[B] = carry;
+    meta[0] = carry < G_max ? carry : G_max;
+    meta[1] = carry;
+  }
+  __syncthreads();
+  const long long P = carry;
+  const int G = P < G_max ? (int)P : G_max;
+  // pass 2: splits per sequence and their slot bases
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int b = base + threadIdx.x;
+    int ns = 0;
+    if (b < B) {
+      const long long c0 = split_of_page(prefix[b], P, G);
+      const long long c1 = split_of_page(prefix[b + 1] - 1, P, G);
+      first_split[b] = (int)c0;
+      ns = (int)(c1 - c0 + 1);
+    }
+    int ex;
+    const int tot = block_exclusive_scan(ns, &ex, tmp);
+    if (b < B) slot_base[b] = carry + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) slot_base[B] = carry;
+}
+
+__global__ void selftest_wait_kernel(int spin_limit, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) mbar_init(&bar, 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the bounded wait must give up.
+    const bool done = mbar_wait(&bar, 0, status, 424242, spin_limit, 200000000ull);
+    (void)done;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_inval(&bar);
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+// KV splits: enough to fill the SMs with the attention kernel's CTAs, never
+// more than there are pages.
+static int choose_splits(const mla_ctx* ctx, int B, int T, int max_pages) {
+  const long long pages_bound = (long long)B * max_pages;
+  int G;
+  if (ctx->cfg.dtype == MLA_BF16) {
+    // one CTA per (split, query token, half of d_latent), one CTA per SM
+    G = ctx->num_sms / (2 * T);
+  } else {
+    const int groups = (ctx->cfg.n_heads + 7) / 8;
+    G = (2 * ctx->num_sms + T * groups - 1) / (T * groups);
+  }
+  if (G < 1) G = 1;
+  if (G > pages_bound) G = (int)pages_bound;
+  return G;
+}
+
+WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages) {
+  const mla_config& c = ctx->cfg;
+  const size_t es = c.dtype == MLA_BF16 ? 2 : 4;
+  const size_t M = (size_t)B * T;
+  const size_t R = (size_t)c.d_latent + c.d_rope;
+  WsLayout L{};
+  L.G = choose_splits(ctx, B, T, max_pages);
+  L.n_slots = L.G + B;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+  L.lens = take(sizeof(int) * B);
+  L.page_prefix = take(sizeof(int) * (B + 1));
+  L.first_split = take(sizeof(int) * B);
+  L.slot_base = take(sizeof(int) * (B + 1));
+  L.meta = take(sizeof(int) * 4);
+  L.qfull = take(es * M * c.n_heads * R);
+  L.part_o = take(sizeof(float) * L.n_slots * T * c.n_heads * c.d_latent);
+  L.part_lse = take(sizeof(float) * L.n_slots * T * c.n_heads);
+  L.o_lat = take(es * M * c.n_heads * c.d_latent);
+  L.o = take(es * M * c.n_heads * c.d_v);
+  L.total = off;
+  return L;
+}
+
+void launch_plan(const mla_ctx* ctx, const WsLayout& L, char* ws, const int32_t* seq_lens,
+                 int B, int T, int max_pages, cudaStream_t st) {
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(
+      seq_lens, B, T, ctx->cfg.page_size, max_pages, ctx->cfg.max_position, L.G,
+      reinterpret_cast<int*>(ws + L.lens), reinterpret_cast<int*>(ws + L.page_prefix),
+      reinterpret_cast<int*>(ws + L.first_split), reinterpret_cast<int*>(ws + L.slot_base),
+      reinterpret_cast<int*>(ws + L.meta), ctx->status);
+}
+
+void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(spin_limit, ctx->status);
+}
+
+}  // namespace mla

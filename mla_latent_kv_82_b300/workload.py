@@ -1,0 +1,82 @@
+"""Device state for one decode workload: weights, paged pool, prefill, step.
+
+Builds everything a decode step needs on one GPU from a seeded
+``synth.workloads.Workload`` and drives the library through ``MLA``:
+weights and queries come from the seeded generator (on the device), the
+pool is prefilled by chunked ``mla_compress_append`` calls, and ``step()``
+is one pass of the hot path: append the T new tokens of every sequence,
+then decode them.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import MLA
+
+W_NAMES = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o")
+
+
+class DeviceState:
+    def __init__(self, wl, device: int = 0, prefill: bool = True, chunk: int = 32768,
+                 sentinel: float | None = None, block_table=None):
+        self.wl = wl
+        self.dev = torch.device("cuda", device)
+        d = wl.dims
+        dt = wl.torch_dtype
+        self.weights = {n: wl.weight(n, device=self.dev) for n in W_NAMES}
+        self.mla = MLA(d, self.weights, wl.dtype, max_position=max(wl.seq_lens), device=device)
+        bt = wl.block_table() if block_table is None else block_table
+        self.bt = torch.as_tensor(bt, dtype=torch.int32, device=self.dev).contiguous()
+        self.num_pages = int(self.bt.max().item()) + 1
+        rows = self.num_pages * d.page_size
+        if sentinel is None:
+            self.cache = torch.empty((rows, d.row_width), dtype=dt, device=self.dev)
+        else:
+            self.cache = torch.full((rows, d.row_width), sentinel, dtype=dt, device=self.dev)
+        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=self.dev)
+        self.q = wl.q(device=self.dev).contiguous()
+        T = wl.T
+        self.h_new = torch.cat([wl.h_rows(b, L, L + T, device=self.dev)
+                                for b, L in enumerate(wl.lens)]).contiguous()
+        self.pos_new = torch.tensor([L + t for L in wl.lens for t in range(T)],
+                                    dtype=torch.int32, device=self.dev)
+        self.out = torch.empty((wl.B, T, d.d_model), dtype=dt, device=self.dev)
+        self.ws_bytes = self.mla.workspace_size(wl.B, T, self.bt.shape[1])
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
+        self.chunk = chunk
+        if prefill:
+            self.prefill()
+
+    def prefill(self):
+        """Append cached tokens 0..lens[b]-1 of every sequence, in chunks."""
+        for b, L in enumerate(self.wl.lens):
+            for p0 in range(0, L, self.chunk):
+                p1 = min(L, p0 + self.chunk)
+                h = self.wl.h_rows(b, p0, p1, device=self.dev)
+                pos = torch.arange(p0, p1, dtype=torch.int32, device=self.dev)
+                self.mla.compress_append(h, pos, self.bt[b:b + 1], self.cache, 1, p1 - p0)
+
+    def append_new(self, stream=None):
+        self.mla.compress_append(self.h_new, self.pos_new, self.bt, self.cache, self.wl.B,
+                                 self.wl.T, stream=stream)
+
+    def decode(self, stream=None):
+        self.mla.decode(self.q, self.cache, self.bt, self.seq_lens, self.out, self.ws,
+                        stream=stream)
+
+    def step(self, stream=None):
+        self.append_new(stream)
+        self.decode(stream)
+
+    def workspace_view(self, which: str) -> torch.Tensor:
+        """o_lat [B*T, n_h, d_c] or o [B*T, n_h*d_v] left in the workspace by decode."""
+        from . import mla_decode_workspace_offsets
+        d, B, T = self.wl.dims, self.wl.B, self.wl.T
+        st, off_lat, off_o = mla_decode_workspace_offsets(self.mla.ctx, B, T, self.bt.shape[1])
+        assert st == 0
+        es = 2 if self.wl.dtype == "bf16" else 4
+        if which == "o_lat":
+            n, off, shape = B * T * d.n_heads * d.d_latent, off_lat, (B * T, d.n_heads, d.d_latent)
+        else:
+            n, off, shape = B * T * d.n_heads * d.d_v, off_o, (B * T, d.n_heads * d.d_v)
+        return self.ws[off:off + n * es].view(self.wl.torch_dtype).view(*shape)
