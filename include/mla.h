@@ -61,7 +61,7 @@ typedef enum { MLA_BF16 = 0, MLA_FP32 = 1 } mla_dtype;
 
 /* Model widths.  bf16 contexts run the tensor-core kernels and need the
  * DeepSeek-V2 head widths: n_heads 128, d_nope 128, d_v 128, d_latent 512,
- * d_rope 64, page_size 64, and d_model a multiple of 64 (<= 16384).
+ * d_rope 64, page_size 64, and d_model a multiple of 128 (<= 16384).
  * fp32 contexts run plain fp32 kernels for small widths: n_heads <= 128,
  * d_latent <= 512, d_latent + d_rope <= 576, d_rope even, d_nope, d_v
  * <= 512, any page_size >= 1.  softmax_scale is applied to q.k; the pages

@@ -34,7 +34,7 @@ mla_status validate_config(const mla_config* c) {
   if (c->max_position > (1 << 26)) return MLA_ERR_UNSUPPORTED;
   if (c->dtype == MLA_BF16) {
     if (c->n_heads != 128 || c->d_nope != 128 || c->d_v != 128 || c->d_latent != 512 ||
-        c->d_rope != 64 || c->page_size != 64 || c->d_model % 64 != 0 || c->d_model > 16384)
+        c->d_rope != 64 || c->page_size != 64 || c->d_model % 128 != 0 || c->d_model > 16384)
       return MLA_ERR_UNSUPPORTED;
   } else if (c->dtype == MLA_FP32) {
     if (c->n_heads > 128 || c->d_latent > 512 || c->d_latent + c->d_rope > 576 ||
@@ -128,6 +128,13 @@ mla_status mla_create(const mla_config* cfg, const mla_weights* w, int device, m
     delete ctx;
     return MLA_ERR_CUDA;
   }
+  if (cfg->dtype == MLA_BF16 && !mla::bf16_setup(ctx)) {
+    mla::bf16_teardown(ctx);
+    cudaFree(ctx->rope_cs);
+    cudaFree(ctx->status);
+    delete ctx;
+    return MLA_ERR_CUDA;
+  }
   *out = ctx;
   return MLA_OK;
 }
@@ -137,6 +144,7 @@ mla_status mla_destroy(mla_ctx* ctx) {
   DeviceGuard g(ctx->device);
   cudaDeviceSynchronize();
   mla_profile_enable(ctx, 0);
+  mla::bf16_teardown(ctx);
   cudaFree(ctx->rope_cs);
   cudaFree(ctx->status);
   delete ctx;
@@ -155,8 +163,9 @@ mla_status mla_compress_append(mla_ctx* ctx, const void* h, int batch, int T,
   DeviceGuard g(ctx->device);
   if (!g.ok) return MLA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool launched = true;
   if (ctx->cfg.dtype == MLA_BF16) {
-    mla::bf16_compress_append(ctx, static_cast<const __nv_bfloat16*>(h), batch, T, positions,
+    launched = mla::bf16_compress_append(ctx, static_cast<const __nv_bfloat16*>(h), batch, T, positions,
                               block_table, max_pages, static_cast<__nv_bfloat16*>(cache),
                               num_pages, st);
   } else {
@@ -164,6 +173,7 @@ mla_status mla_compress_append(mla_ctx* ctx, const void* h, int batch, int T,
                              block_table, max_pages, static_cast<float*>(cache), num_pages, st);
   }
   mla::prof_mark(ctx, st, nullptr);
+  if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return launch_status();
 }
 
@@ -203,8 +213,9 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache, int num_pa
   mla::prof_mark(ctx, st, "plan");
   mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
   ctx->launches += 1;
+  bool launched = true;
   if (ctx->cfg.dtype == MLA_BF16) {
-    mla::bf16_decode(ctx, static_cast<const __nv_bfloat16*>(q),
+    launched = mla::bf16_decode(ctx, static_cast<const __nv_bfloat16*>(q),
                      static_cast<const __nv_bfloat16*>(cache), num_pages, block_table, max_pages,
                      batch, T, static_cast<__nv_bfloat16*>(out), ws, L, st);
   } else {
@@ -213,6 +224,7 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache, int num_pa
                     L, st);
   }
   mla::prof_mark(ctx, st, nullptr);
+  if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return launch_status();
 }
 

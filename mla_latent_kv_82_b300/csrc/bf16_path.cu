@@ -1,0 +1,296 @@
+// bf16 decode step at DeepSeek-V2 head widths: launches and small kernels.
+//
+//   append   : wgemm [W^DKV; W^KR] h  (+RoPE, paged 16-byte stores)
+//   decode   : plan -> wgemm absorb (query image) -> attend (split-KV)
+//              -> combine (o_lat, bf16) -> wgemm W^UV -> wgemm W_O
+// Every launch after the first of a call uses programmatic dependent launch.
+#include <algorithm>
+
+#include "layouts.cuh"
+#include "tmap.h"
+#include "wgemm.h"
+#include "device_util.cuh"
+
+namespace mla {
+namespace {
+
+// Merge the split partials of one (token, head) into o_lat = sum_s w_s O_s /
+// sum_s w_s with w_s = 2^(lse_s - max lse): the log-sum-exp combine of
+// flash-decoding.  One warp per (token, head); lane owns 16 latent columns.
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+               const int* __restrict__ slot_base, int T, int M,
+               __nv_bfloat16* __restrict__ o_lat) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= M * kHeads) return;
+  const int m = gw / kHeads, head = gw % kHeads;
+  const int b = m / T, t = m % T;
+  const int s0 = slot_base[b], s1 = slot_base[b + 1];
+  float lmax = -INFINITY;
+  for (int s = s0; s < s1; ++s) lmax = fmaxf(lmax, part_lse[((size_t)s * T + t) * kHeads + head]);
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float wsum = 0.f;
+  for (int s = s0; s < s1; ++s) {
+    const size_t r = ((size_t)s * T + t) * kHeads + head;
+    const float w = exp2f(part_lse[r] - lmax);
+    if (w == 0.f) continue;
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(part_o + r * kLat) + lane * 4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 x = src[k];
+      acc[4 * k] = fmaf(w, x.x, acc[4 * k]);
+      acc[4 * k + 1] = fmaf(w, x.y, acc[4 * k + 1]);
+      acc[4 * k + 2] = fmaf(w, x.z, acc[4 * k + 2]);
+      acc[4 * k + 3] = fmaf(w, x.w, acc[4 * k + 3]);
+    }
+  }
+  const float inv = 1.f / wsum;
+  __align__(16) __nv_bfloat16 outv[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) outv[k] = __float2bfloat16_rn(acc[k] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)m * kHeads + head) * kLat + lane * 16);
+  dst[0] = reinterpret_cast<const uint4*>(outv)[0];
+  dst[1] = reinterpret_cast<const uint4*>(outv)[1];
+}
+
+// K splits so that one wave fills the SMs, within the scratch budget.
+int choose_k_splits(const mla_ctx* ctx, int m_tiles, int n_tiles, int nt, int k_chunks,
+                    size_t partial_cap) {
+  const int target = ctx->num_sms * wgemm_ctas_per_sm(nt);
+  int s = target / std::max(1, m_tiles * n_tiles);
+  s = std::max(1, std::min(s, k_chunks));
+  while (s > 1 && (size_t)m_tiles * n_tiles * s * nt * 128 * sizeof(float) > partial_cap) --s;
+  return s;
+}
+
+struct Bf16Plans {
+  int nt, n_tiles;
+  int s_uv, s_o;
+};
+
+Bf16Plans decode_plans(const mla_ctx* ctx, int M) {
+  Bf16Plans p;
+  p.nt = wgemm_token_tile(M);
+  p.n_tiles = (M + p.nt - 1) / p.nt;
+  const size_t big = (size_t)1 << 40;
+  p.s_uv = choose_k_splits(ctx, kHeads, p.n_tiles, p.nt, kLat / 64, big);
+  p.s_o = choose_k_splits(ctx, ctx->cfg.d_model / 128, p.n_tiles, p.nt, kHeads * kDv / 64, big);
+  // keep the scratch of the largest-M cases bounded
+  const size_t cap = 64u << 20;
+  while (p.s_o > 1 && (size_t)(ctx->cfg.d_model / 128) * p.n_tiles * p.s_o * p.nt * 512 > cap)
+    --p.s_o;
+  while (p.s_uv > 1 && (size_t)kHeads * p.n_tiles * p.s_uv * p.nt * 512 > cap) --p.s_uv;
+  return p;
+}
+
+WgArgs base_args(const mla_ctx* ctx) {
+  WgArgs a{};
+  a.status = ctx->status;
+  a.counters = ctx->counters;
+  a.rope_cs = ctx->rope_cs;
+  a.max_position = ctx->cfg.max_position;
+  a.tiles_per_head = 1;
+  a.valid_rows_last = 128;
+  a.splits = 1;
+  return a;
+}
+
+bool check(cudaError_t e) {
+  if (e != cudaSuccess) return false;
+  return true;
+}
+
+}  // namespace
+
+size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M) {
+  const Bf16Plans p = decode_plans(ctx, M);
+  const size_t uv = (size_t)kHeads * p.n_tiles * p.s_uv * p.nt * 128 * sizeof(float);
+  const size_t o = (size_t)(ctx->cfg.d_model / 128) * p.n_tiles * p.s_o * p.nt * 128 *
+                   sizeof(float);
+  return std::max(uv, o);
+}
+
+bool bf16_setup(mla_ctx* ctx) {
+  const int D = ctx->cfg.d_model;
+  const mla_weights& w = ctx->w;
+  bool ok = make_tmap_bf16_2d(&ctx->tm_wdkv, w.w_dkv, kLat, D, D, 64, 128, true) &&
+            make_tmap_bf16_2d(&ctx->tm_wkr, w.w_kr, kRope, D, D, 64, 128, true) &&
+            make_tmap_bf16_2d(&ctx->tm_wuk, w.w_uk, kHeads * kNope, kLat, kLat, 64, 64, true) &&
+            make_tmap_bf16_2d(&ctx->tm_wuv, w.w_uv, kHeads * kDv, kLat, kLat, 64, 128, true) &&
+            make_tmap_bf16_2d(&ctx->tm_wo, w.w_o, D, kHeads * kDv, kHeads * kDv, 64, 128, true);
+  if (!ok) return false;
+  if (cudaMalloc(&ctx->append_partials, kAppendPartialBytes) != cudaSuccess ||
+      cudaMalloc(&ctx->counters, kCounters * sizeof(int)) != cudaSuccess ||
+      cudaMemset(ctx->counters, 0, kCounters * sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+void bf16_teardown(mla_ctx* ctx) {
+  if (ctx->append_partials) cudaFree(ctx->append_partials);
+  if (ctx->counters) cudaFree(ctx->counters);
+  ctx->append_partials = nullptr;
+  ctx->counters = nullptr;
+}
+
+bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
+                          const int32_t* pos, const int32_t* bt, int max_pages,
+                          __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
+  const int M = B * T, D = ctx->cfg.d_model;
+  WgPlan p{};
+  p.nt = wgemm_token_tile(M);
+  p.n_tiles = (M + p.nt - 1) / p.nt;
+  if (p.n_tiles > 65535) return false;
+  p.m_tiles = 5;   // 4 tiles of W^DKV rows, 1 tile of W^KR rows
+  p.tmA = ctx->tm_wdkv;
+  p.tmA2 = ctx->tm_wkr;
+  if (!make_tmap_bf16_2d(&p.tmB, h, M, D, D, 64, p.nt, false)) {
+    cudaGetLastError();
+    return false;
+  }
+  WgArgs& a = p.args;
+  a = base_args(ctx);
+  a.n_tokens = M;
+  a.k_chunks = D / 64;
+  a.splits = choose_k_splits(ctx, p.m_tiles * 1, p.n_tiles, p.nt, a.k_chunks, kAppendPartialBytes);
+  a.tiles_per_head = 5;
+  a.a_tiles_main = 4;
+  a.valid_rows_last = kRope;
+  a.cache = cache;
+  a.pos = pos;
+  a.bt = bt;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.T = T;
+  a.append_rope_tile = 4;
+  a.partials = ctx->append_partials;
+  prof_mark(ctx, st, "compress_append");
+  ctx->launches += 1;
+  return check(wgemm_launch(p, WG_APPEND, false, st, true));
+}
+
+bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+                 int num_pages, const int32_t* bt, int max_pages, int B, int T,
+                 __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st) {
+  const int M = B * T, D = ctx->cfg.d_model;
+  const Bf16Plans bp = decode_plans(ctx, M);
+  if (bp.n_tiles > 65535) return false;
+  __nv_bfloat16* qimg = reinterpret_cast<__nv_bfloat16*>(ws + L.qfull);
+  __nv_bfloat16* olat = reinterpret_cast<__nv_bfloat16*>(ws + L.o_lat);
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ws + L.o);
+  float* part = reinterpret_cast<float*>(ws + L.wg_part);
+
+  // ---- absorbed query: W^UK_i^T q^C_i (+ rotated q^R) -> query image
+  {
+    WgPlan p{};
+    p.nt = bp.nt;
+    p.n_tiles = bp.n_tiles;
+    p.m_tiles = kHeads * (kLat / 128);
+    p.tmA = ctx->tm_wuk;
+    p.tmA2 = ctx->tm_wuk;
+    if (!make_tmap_bf16_2d(&p.tmB, q, M, kHeads * (kNope + kRope), kHeads * (kNope + kRope), 64,
+                           p.nt, false)) {
+      cudaGetLastError();
+      return false;
+    }
+    WgArgs& a = p.args;
+    a = base_args(ctx);
+    a.n_tokens = M;
+    a.k_chunks = kNope / 64;
+    a.tiles_per_head = kLat / 128;
+    a.a_head_rows = kNope;
+    a.b_head_cols = kNope + kRope;
+    a.qimg = qimg;
+    a.q = q;
+    a.lens = reinterpret_cast<const int*>(ws + L.lens);
+    a.T = T;
+    prof_mark(ctx, st, "absorb_q");
+    ctx->launches += 1;
+    if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
+  }
+  // ---- split-KV attention over the latent cache
+  simt_attend_bf16_img(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st);
+  // ---- log-sum-exp combine -> o_lat (bf16)
+  {
+    prof_mark(ctx, st, "combine");
+    ctx->launches += 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((M * kHeads + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!check(cudaLaunchKernelEx(&cfg, combine_kernel,
+                                  (const float*)reinterpret_cast<float*>(ws + L.part_o),
+                                  (const float*)reinterpret_cast<float*>(ws + L.part_lse),
+                                  (const int*)reinterpret_cast<int*>(ws + L.slot_base), T, M,
+                                  olat)))
+      return false;
+  }
+  // ---- value up-projection: o_i = W^UV_i o_lat_i
+  {
+    WgPlan p{};
+    p.nt = bp.nt;
+    p.n_tiles = bp.n_tiles;
+    p.m_tiles = kHeads;
+    p.tmA = ctx->tm_wuv;
+    p.tmA2 = ctx->tm_wuv;
+    if (!make_tmap_bf16_2d(&p.tmB, olat, M, kHeads * kLat, kHeads * kLat, 64, p.nt, false)) {
+      cudaGetLastError();
+      return false;
+    }
+    WgArgs& a = p.args;
+    a = base_args(ctx);
+    a.n_tokens = M;
+    a.k_chunks = kLat / 64;
+    a.splits = bp.s_uv;
+    a.tiles_per_head = 1;
+    a.a_head_rows = kDv;
+    a.b_head_cols = kLat;
+    a.out = o;
+    a.ld_out = kHeads * kDv;
+    a.out_head_cols = kDv;
+    a.partials = part;
+    prof_mark(ctx, st, "value_proj");
+    ctx->launches += 1;
+    if (!check(wgemm_launch(p, WG_ROWMAJOR, false, st, true))) return false;
+  }
+  // ---- output projection: u = W_O o
+  {
+    WgPlan p{};
+    p.nt = bp.nt;
+    p.n_tiles = bp.n_tiles;
+    p.m_tiles = D / 128;
+    p.tmA = ctx->tm_wo;
+    p.tmA2 = ctx->tm_wo;
+    if (!make_tmap_bf16_2d(&p.tmB, o, M, kHeads * kDv, kHeads * kDv, 64, p.nt, false)) {
+      cudaGetLastError();
+      return false;
+    }
+    WgArgs& a = p.args;
+    a = base_args(ctx);
+    a.n_tokens = M;
+    a.k_chunks = kHeads * kDv / 64;
+    a.splits = bp.s_o;
+    a.tiles_per_head = D / 128;
+    a.out = out;
+    a.ld_out = D;
+    a.out_head_cols = 0;
+    a.partials = part;
+    prof_mark(ctx, st, "out_proj");
+    ctx->launches += 1;
+    if (!check(wgemm_launch(p, WG_ROWMAJOR, false, st, true))) return false;
+  }
+  return true;
+}
+
+}  // namespace mla

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstddef>
@@ -19,6 +20,10 @@ struct mla_ctx {
   float2* rope_cs;     // device [max_position, d_rope/2] of (cos, sin)
   int* status;         // device [MLA_ST_WORDS]
   int64_t launches;
+  // bf16 path: TMA maps of the weights, split-K scratch of the append
+  CUtensorMap tm_wdkv, tm_wkr, tm_wuk, tm_wuv, tm_wo;
+  float* append_partials = nullptr;   // kAppendPartialBytes
+  int* counters = nullptr;            // kCounters, zero between launches
   // per-kernel timing (mla_profile_enable)
   bool prof = false;
   int n_marks = 0;
@@ -27,6 +32,9 @@ struct mla_ctx {
 };
 
 namespace mla {
+
+constexpr size_t kAppendPartialBytes = 8u << 20;
+constexpr int kCounters = 65536;
 
 // Byte layout of the decode workspace (all offsets 256-byte aligned).
 struct WsLayout {
@@ -39,6 +47,7 @@ struct WsLayout {
   size_t part_lse; // fp32 [n_slots, T, n_heads] (log2 domain)
   size_t o_lat;    // dtype [batch*T, n_heads, d_latent]
   size_t o;        // dtype [batch*T, n_heads*d_v]
+  size_t wg_part;  // fp32 split-K partials of the value / output projections
   size_t total;
 };
 
@@ -61,12 +70,20 @@ void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,
                 const WsLayout& L, cudaStream_t st);
 
 // bf16 kernels (DeepSeek-V2 head widths).
-void bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
+bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           const int32_t* pos, const int32_t* bt, int max_pages,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st);
-void bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
                  int num_pages, const int32_t* bt, int max_pages, int B, int T,
                  __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
+
+// bf16 path helpers
+bool bf16_setup(mla_ctx* ctx);                 // weight maps + scratch, at create
+void bf16_teardown(mla_ctx* ctx);
+size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M);
+void simt_attend_bf16_img(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
+                          int num_pages, const int32_t* bt, int max_pages, int B, int T,
+                          char* ws, const WsLayout& L, cudaStream_t st);
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
 

@@ -164,6 +164,7 @@ WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages) {
   L.part_lse = take(sizeof(float) * L.n_slots * T * c.n_heads);
   L.o_lat = take(es * M * c.n_heads * c.d_latent);
   L.o = take(es * M * c.n_heads * c.d_v);
+  L.wg_part = take(c.dtype == MLA_BF16 ? bf16_wg_partial_bytes(ctx, (int)M) : 0);
   L.total = off;
   return L;
 }

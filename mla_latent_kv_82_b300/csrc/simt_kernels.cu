@@ -9,6 +9,7 @@
 //   combine_uv       log-sum-exp merge of the splits, o_i = W^UV_i o~_i
 //   out_proj         u = W_O [o_1; ...; o_{n_h}]
 #include "device_util.cuh"
+#include "layouts.cuh"
 
 namespace mla {
 namespace {
@@ -141,7 +142,7 @@ constexpr int kAttWarps = 8, kAttRows = 8, kMaxR = 576, kMaxRegs = kMaxR / 32, k
 
 // One CTA per (split, query token, group of 8 heads); one warp per head.
 // Online softmax in the log2 domain; writes O/l and m + log2(l) per split.
-template <typename T>
+template <typename T, bool IMG>
 __global__ void __launch_bounds__(kAttWarps * 32)
 attend_kernel(const T* __restrict__ Q, const T* __restrict__ cache, int num_pages,
               const int32_t* __restrict__ bt, int max_pages, const int* __restrict__ lens,
@@ -172,7 +173,13 @@ attend_kernel(const T* __restrict__ Q, const T* __restrict__ cache, int num_page
 #pragma unroll
     for (int k = 0; k < kMaxRegs; ++k) {
       const int f = lane + 32 * k;
-      qr[k] = (active && f < R) ? to_f(Q[(mrow * H + head) * R + f]) : 0.f;
+      float qv = 0.f;
+      if (active && f < R) {
+        qv = IMG ? to_f(*reinterpret_cast<const T*>(reinterpret_cast<const char*>(Q) +
+                                                    mrow * kQImgBytes + qimg_off(head, f)))
+                 : to_f(Q[(mrow * H + head) * R + f]);
+      }
+      qr[k] = qv;
     }
     float acc[kMaxC];
 #pragma unroll
@@ -311,7 +318,7 @@ void decode_impl(mla_ctx* ctx, const T* q, const T* cache, int num_pages,
   const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
   prof_mark(ctx, st, "attend");
   ctx->launches += 1;
-  attend_kernel<T><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps), kAttWarps * 32, 0, st>>>(
+  attend_kernel<T, false><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps), kAttWarps * 32, 0, st>>>(
       Q, cache, num_pages, bt, max_pages, lens, prefix, first, sbase, meta, B, T_, H,
       c.d_latent, c.d_rope, c.page_size, scale_log2, po, pl, ctx->status);
   prof_mark(ctx, st, "combine_uv");
@@ -341,17 +348,24 @@ void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,
   decode_impl<float>(ctx, q, cache, num_pages, bt, max_pages, B, T, out, ws, L, st);
 }
 
-// First bf16 path: the same SIMT kernels on bf16 storage.
-void bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
-                          const int32_t* pos, const int32_t* bt, int max_pages,
-                          __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
-  compress_append_impl<__nv_bfloat16>(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, st);
-}
-
-void bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
-                 int num_pages, const int32_t* bt, int max_pages, int B, int T,
-                 __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st) {
-  decode_impl<__nv_bfloat16>(ctx, q, cache, num_pages, bt, max_pages, B, T, out, ws, L, st);
+// bf16 attention over the query image (stand-in until the tensor-core kernel).
+void simt_attend_bf16_img(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
+                          int num_pages, const int32_t* bt, int max_pages, int B, int T_,
+                          char* ws, const WsLayout& L, cudaStream_t st) {
+  const mla_config& c = ctx->cfg;
+  const int H = c.n_heads;
+  const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  prof_mark(ctx, st, "attend");
+  ctx->launches += 1;
+  attend_kernel<__nv_bfloat16, true><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps),
+                                       kAttWarps * 32, 0, st>>>(
+      qimg, cache, num_pages, bt, max_pages, reinterpret_cast<const int*>(ws + L.lens),
+      reinterpret_cast<const int*>(ws + L.page_prefix),
+      reinterpret_cast<const int*>(ws + L.first_split),
+      reinterpret_cast<const int*>(ws + L.slot_base), reinterpret_cast<const int*>(ws + L.meta),
+      B, T_, H, c.d_latent, c.d_rope, c.page_size, scale_log2,
+      reinterpret_cast<float*>(ws + L.part_o), reinterpret_cast<float*>(ws + L.part_lse),
+      ctx->status);
 }
 
 }  // namespace mla

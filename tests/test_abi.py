@@ -45,6 +45,7 @@ def test_create_validates_before_any_cuda_call():
     assert m.mla_create(_cfg(m, n_heads=64), w, 0)[0] == m.MLA_ERR_UNSUPPORTED
     assert m.mla_create(_cfg(m, d_latent=256), w, 0)[0] == m.MLA_ERR_UNSUPPORTED
     assert m.mla_create(_cfg(m, d_model=5000), w, 0)[0] == m.MLA_ERR_UNSUPPORTED
+    assert m.mla_create(_cfg(m, d_model=5120 + 64), w, 0)[0] == m.MLA_ERR_UNSUPPORTED
     assert m.mla_create(_cfg(m, d_rope=7), w, 0)[0] == m.MLA_ERR_INVALID_ARG
     assert m.mla_create(_cfg(m, softmax_scale=0.0), w, 0)[0] == m.MLA_ERR_INVALID_ARG
     assert m.mla_create(_cfg(m, dtype=7), w, 0)[0] == m.MLA_ERR_INVALID_ARG
