@@ -215,7 +215,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
   }
   // ---- split-KV attention over the latent cache
-  simt_attend_bf16_img(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st);
+  if (!tc_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) return false;
   // ---- log-sum-exp combine -> o_lat (bf16)
   {
     prof_mark(ctx, st, "combine");

@@ -81,9 +81,9 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
 bool bf16_setup(mla_ctx* ctx);                 // weight maps + scratch, at create
 void bf16_teardown(mla_ctx* ctx);
 size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M);
-void simt_attend_bf16_img(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
-                          int num_pages, const int32_t* bt, int max_pages, int B, int T,
-                          char* ws, const WsLayout& L, cudaStream_t st);
+bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
+               int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
+               const WsLayout& L, cudaStream_t st);
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
 

@@ -1,15 +1,15 @@
 // Plain SIMT kernels for every step of MLA decode, for any small widths.
 //
-// These serve fp32 contexts (fp32 FMA throughout: the tensor cores cannot
-// meet an fp32 tolerance).  Steps, following the page "DeepSeek-V2：在“大力出
-// 奇迹”的AI军备竞赛中，四两拨千斤" (liang.world), 第二章 §1-§3:
+// These serve fp32 contexts only (fp32 FMA throughout: the tensor cores
+// cannot meet an fp32 tolerance); bf16 contexts run the tcgen05 kernels.
+// Steps, following the page "DeepSeek-V2：在“大力出奇迹”的AI军备竞赛中，四两拨
+// 千斤" (liang.world), 第二章 §1-§3:
 //   compress_append  [c ; k^R] = [W^DKV h ; RoPE_pos(W^KR h)] -> paged pool
 //   absorb_q         q~_i = W^UK_i^T q^C_i, q^R_i rotated at its position
 //   attend           split-KV online softmax over the latent rows
 //   combine_uv       log-sum-exp merge of the splits, o_i = W^UV_i o~_i
 //   out_proj         u = W_O [o_1; ...; o_{n_h}]
 #include "device_util.cuh"
-#include "layouts.cuh"
 
 namespace mla {
 namespace {
@@ -142,7 +142,7 @@ constexpr int kAttWarps = 8, kAttRows = 8, kMaxR = 576, kMaxRegs = kMaxR / 32, k
 
 // One CTA per (split, query token, group of 8 heads); one warp per head.
 // Online softmax in the log2 domain; writes O/l and m + log2(l) per split.
-template <typename T, bool IMG>
+template <typename T>
 __global__ void __launch_bounds__(kAttWarps * 32)
 attend_kernel(const T* __restrict__ Q, const T* __restrict__ cache, int num_pages,
               const int32_t* __restrict__ bt, int max_pages, const int* __restrict__ lens,
@@ -173,13 +173,7 @@ attend_kernel(const T* __restrict__ Q, const T* __restrict__ cache, int num_page
 #pragma unroll
     for (int k = 0; k < kMaxRegs; ++k) {
       const int f = lane + 32 * k;
-      float qv = 0.f;
-      if (active && f < R) {
-        qv = IMG ? to_f(*reinterpret_cast<const T*>(reinterpret_cast<const char*>(Q) +
-                                                    mrow * kQImgBytes + qimg_off(head, f)))
-                 : to_f(Q[(mrow * H + head) * R + f]);
-      }
-      qr[k] = qv;
+      qr[k] = (active && f < R) ? to_f(Q[(mrow * H + head) * R + f]) : 0.f;
     }
     float acc[kMaxC];
 #pragma unroll
@@ -318,7 +312,7 @@ void decode_impl(mla_ctx* ctx, const T* q, const T* cache, int num_pages,
   const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
   prof_mark(ctx, st, "attend");
   ctx->launches += 1;
-  attend_kernel<T, false><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps), kAttWarps * 32, 0, st>>>(
+  attend_kernel<T><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps), kAttWarps * 32, 0, st>>>(
       Q, cache, num_pages, bt, max_pages, lens, prefix, first, sbase, meta, B, T_, H,
       c.d_latent, c.d_rope, c.page_size, scale_log2, po, pl, ctx->status);
   prof_mark(ctx, st, "combine_uv");
@@ -346,26 +340,6 @@ void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,
                 const int32_t* bt, int max_pages, int B, int T, float* out, char* ws,
                 const WsLayout& L, cudaStream_t st) {
   decode_impl<float>(ctx, q, cache, num_pages, bt, max_pages, B, T, out, ws, L, st);
-}
-
-// bf16 attention over the query image (stand-in until the tensor-core kernel).
-void simt_attend_bf16_img(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
-                          int num_pages, const int32_t* bt, int max_pages, int B, int T_,
-                          char* ws, const WsLayout& L, cudaStream_t st) {
-  const mla_config& c = ctx->cfg;
-  const int H = c.n_heads;
-  const float scale_log2 = c.softmax_scale * 1.4426950408889634f;
-  prof_mark(ctx, st, "attend");
-  ctx->launches += 1;
-  attend_kernel<__nv_bfloat16, true><<<dim3(L.G, T_, (H + kAttWarps - 1) / kAttWarps),
-                                       kAttWarps * 32, 0, st>>>(
-      qimg, cache, num_pages, bt, max_pages, reinterpret_cast<const int*>(ws + L.lens),
-      reinterpret_cast<const int*>(ws + L.page_prefix),
-      reinterpret_cast<const int*>(ws + L.first_split),
-      reinterpret_cast<const int*>(ws + L.slot_base), reinterpret_cast<const int*>(ws + L.meta),
-      B, T_, H, c.d_latent, c.d_rope, c.page_size, scale_log2,
-      reinterpret_cast<float*>(ws + L.part_o), reinterpret_cast<float*>(ws + L.part_lse),
-      ctx->status);
 }
 
 }  // namespace mla

@@ -101,6 +101,14 @@ def test_append_placement_is_exact_and_untouched_rows_keep_sentinel():
         check(to_np(pool_rows_of(st, b)), rows, "bf16", f"rows b={b}")
 
 
+@pytest.mark.parametrize("T,lens", [(1, [0, 5, 33, 64, 100]), (2, [1, 31, 62, 200])])
+def test_stale_pool_rows_do_not_leak(T, lens):
+    """Rows of the pool that no sequence owns hold NaN: outputs stay exact."""
+    st = _run(small_bf16(lens, T), sentinel=float("nan"))
+    assert torch.isfinite(st.out.float()).all()
+    _compare_all(st, "explicit")
+
+
 def test_shuffled_block_table_is_bitwise_identical():
     wl = small_bf16([70, 200, 5, 130], 1, shuffle=True)
     a = _run(wl)
