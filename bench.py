@@ -3,10 +3,11 @@
 
 One step = one pass of the whole hot path over the workload's batch:
 compress + RoPE + paged append of the T new tokens of every sequence, then
-the absorbed decode (query absorption, split-KV attention, combine + W^UV,
-W_O).  Inputs and state are resident in HBM when the timed region starts;
-L2 is flushed (a 2x-L2 buffer is written) before every timed step, outside
-the step's own CUDA-event bracket.
+the absorbed decode (query absorption, split-KV attention, combine, W^UV,
+W_O), replayed as one CUDA graph.  Inputs and state are resident in HBM
+when the timed region starts; L2 is flushed (a 2x-L2 buffer is written,
+then another is read) before every timed step, outside the step's own
+CUDA-event bracket.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
                   [--impl mla|reference]
@@ -82,13 +83,17 @@ def work_model(wl):
         "absorb_q": (H * dn * dc * es + M * H * (dn + dr) * es + M * H * R * es,
                      2.0 * M * H * dn * dc),
         "attend": (cache_rows * R * es + M * H * R * es, 2.0 * visible * H * (R + dc)),
+        "combine": (M * H * dc * es, 0.0),
+        "value_proj": (H * dv * dc * es + M * H * dc * es + M * H * dv * es,
+                       2.0 * M * H * dv * dc),
         "combine_uv": (H * dv * dc * es + M * H * dv * es, 2.0 * M * H * dv * dc),
         "out_proj": (D * H * dv * es + M * H * dv * es + M * D * es, 2.0 * M * D * H * dv),
         "plan": (wl.B * 4, 0.0),
     }
     tot_bytes = (R * D + H * dn * dc + H * dv * dc + D * H * dv) * es \
         + cache_rows * R * es + M * (D + H * (dn + dr) + D) * es
-    tot_flops = sum(f for _, f in k.values())
+    tot_flops = sum(k[n][1] for n in ("compress_append", "absorb_q", "attend", "value_proj",
+                                      "out_proj"))
     return k, tot_bytes, tot_flops, cache_rows * R * es
 
 
@@ -259,44 +264,56 @@ def run_mla(a, wl, rank, local_rank, world):
     st = DeviceState(wl, device=local_rank)
     torch.cuda.synchronize()
     l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    # L2 flush: write a 2x-L2 buffer, then read another one, so the timed step
+    # starts with a cold L2 that holds no dirty lines to write back
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=sink)
 
     for _ in range(a.warmup):
-        flush.zero_()
         st.step()
     torch.cuda.synchronize()
     if st.mla.check_status() != 0:
         raise RuntimeError("device status set during warm-up")
+
+    # one decode step (append + decode) as a CUDA graph, replayed every step
+    n0 = st.mla.launch_count()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        st.step()
+    launches_per_step = st.mla.launch_count() - n0
+    for _ in range(a.warmup):
+        flush()
+        g_step.replay()
+    torch.cuda.synchronize()
 
     bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0" \
         if hasattr(props, "pci_bus_id") else str(local_rank)
     clocks = ClockSampler(bus)
     clocks.start()
     time.sleep(0.3)
+    stream = torch.cuda.current_stream()
 
-    m.mla_profile_enable(st.mla.ctx, 1)
-    kt = {}
+    # ---- timed region: K steps, each bracketed by CUDA events, flush outside
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(a.steps)]
-    launches0 = st.mla.launch_count()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for i in range(a.steps):
-        flush.zero_()
+        flush()
         evs[i][0].record(stream)
-        st.step()
+        g_step.replay()
         evs[i][1].record(stream)
-        for name, ms in m.mla_profile_read(st.mla.ctx):
-            kt.setdefault(name, []).append(ms)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    launches = st.mla.launch_count() - launches0
-    m.mla_profile_enable(st.mla.ctx, 0)
     step_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     if world > 1:
         t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
@@ -307,10 +324,26 @@ def run_mla(a, wl, rank, local_rank, world):
         raise RuntimeError(f"device status {status} after the timed region")
     time.sleep(0.2)
     clocks.stop()
+    launches = launches_per_step * a.steps
 
     tokens = wl.B * wl.T * a.steps * world
     value = tokens / (step_ms * 1e-3)
     ms_per_step = step_ms / a.steps
+
+    # ---- per-kernel durations: the same steps with an event at every kernel
+    # boundary (events keep kernels from overlapping, so this pass only
+    # apportions time between kernels; the step time comes from the pass above)
+    m.mla_profile_enable(st.mla.ctx, 1)
+    g_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_prof):
+        st.step()
+    kt = {}
+    for i in range(a.steps):
+        flush()
+        g_prof.replay()
+        for name, ms in m.mla_profile_read(st.mla.ctx):
+            kt.setdefault(name, []).append(ms)
+    m.mla_profile_enable(st.mla.ctx, 0)
 
     # ---- roofline of the dominant kernel and of the whole step
     kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl)
@@ -332,7 +365,9 @@ def run_mla(a, wl, rank, local_rank, world):
                  "traffic": None, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                  if peaks["source"] == "measured" else "fallback",
                  "algorithmic_bytes_per_launch": b_dom, "algorithmic_flops_per_launch": f_dom,
-                 "avg_launch_ms": avg[dom]})
+                 "avg_launch_ms": avg[dom],
+                 "timing": "per-kernel CUDA events on the launching stream, second pass of "
+                           "the same steps"})
     t_step = ms_per_step * 1e-3
     step_roof = max(tot_bytes / (bw_peak * 1e9), tot_flops / (tf_peak * 1e12))
 
@@ -344,21 +379,27 @@ def run_mla(a, wl, rank, local_rank, world):
         p_h = st.pos_new.cpu().pin_memory()
         s_h = st.seq_lens.cpu().pin_memory()
         out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-        e_steps = min(a.steps, 200)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(e_steps)]
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        for i in range(e_steps):
-            flush.zero_()
-            ev[i][0].record(stream)
+
+        def e2e_step():
             st.h_new.copy_(h_h, non_blocking=True)
             st.q.copy_(q_h, non_blocking=True)
             st.pos_new.copy_(p_h, non_blocking=True)
             st.seq_lens.copy_(s_h, non_blocking=True)
             st.step()
             out_h.copy_(st.out, non_blocking=True)
+
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e):
+            e2e_step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(a.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(a.steps):
+            flush()
+            ev[i][0].record(stream)
+            g_e2e.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         e_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
@@ -366,11 +407,11 @@ def run_mla(a, wl, rank, local_rank, world):
             t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
-        e2e = {"value": wl.B * wl.T * e_steps * world / (e_ms * 1e-3), "unit": "tokens/s",
+        e2e = {"value": wl.B * wl.T * a.steps * world / (e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (h_h, q_h, p_h, s_h)),
-               "d2h_bytes_per_step": out_h.numel() * out_h.element_size(), "steps": e_steps,
-               "note": "inputs copied from pinned host memory and the output copied back "
-                       "inside the timed region of every step"}
+               "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+               "note": "every step copies its inputs from pinned host memory and its output "
+                       "back inside the timed region (one CUDA graph per step)"}
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -389,7 +430,10 @@ def run_mla(a, wl, rank, local_rank, world):
         "data": "synthetic: seeded N(0,1) hidden states and queries, N(0,1/fan_in) weights",
         "config": {"workload": wl.name, "batch": wl.B, "T": wl.T,
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
-                   f"({2 * l2 >> 20} MiB write, outside the step's event bracket)",
+                   f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
+                   "step's event bracket)",
+                   "graph": "each step is one CUDA-graph replay of mla_compress_append + "
+                            "mla_decode",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cache_gbs": cache_bytes / t_step / 1e9,
                    "step_algorithmic_gb": tot_bytes / 1e9,

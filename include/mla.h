@@ -167,13 +167,16 @@ int64_t mla_launch_count(const mla_ctx* ctx);
  * of this library takes when it gives up). */
 mla_status mla_selftest_bounded_wait(mla_ctx* ctx, int spin_limit, void* stream);
 
-/* Per-kernel timing for benchmarks.  While enabled, every call records a
- * CUDA event on its stream before each kernel it enqueues and one after the
- * last; mla_profile_read waits for the recorded events and writes, for at
- * most `max_kernels` kernels enqueued since the previous read, the kernel's
- * name (a static string) and its duration in milliseconds.  It returns the
- * number written (or -1 on error) and forgets the recorded events.  At most
- * 64 events are kept between reads; later kernels are not recorded. */
+/* Per-kernel timing for benchmarks.  mla_profile_enable(ctx, 1) starts a
+ * fresh recording: from then on every call records a CUDA event on its
+ * stream before each kernel it enqueues and one after the last (at most 64
+ * events; later kernels are not recorded).  Calls captured into a CUDA
+ * graph record event nodes, so each replay re-times the same kernels.
+ * mla_profile_read waits for the last recorded event and writes, for at
+ * most `max_kernels` recorded kernels, the kernel's name (a static string)
+ * and its duration in milliseconds; it returns the number written or -1.
+ * The events mark kernel boundaries, which keeps a kernel from overlapping
+ * its predecessor: time whole steps with profiling off. */
 mla_status mla_profile_enable(mla_ctx* ctx, int enable);
 int mla_profile_read(mla_ctx* ctx, float* ms, const char** names, int max_kernels);
 

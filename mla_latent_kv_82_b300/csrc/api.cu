@@ -55,7 +55,14 @@ mla_status launch_status() {
 namespace mla {
 void prof_mark(mla_ctx* ctx, cudaStream_t st, const char* name) {
   if (!ctx->prof || ctx->n_marks >= 64) return;
-  if (cudaEventRecord(ctx->marks[ctx->n_marks], st) != cudaSuccess) {
+  // inside stream capture the mark must become an event-record node of the graph
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) cudaGetLastError();
+  const cudaError_t e = cs == cudaStreamCaptureStatusActive
+                            ? cudaEventRecordWithFlags(ctx->marks[ctx->n_marks], st,
+                                                       cudaEventRecordExternal)
+                            : cudaEventRecord(ctx->marks[ctx->n_marks], st);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return;
   }
@@ -251,7 +258,9 @@ mla_status mla_profile_enable(mla_ctx* ctx, int enable) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   if (!g.ok) return MLA_ERR_CUDA;
-  if (enable && !ctx->prof) {
+  if (enable && ctx->prof) {
+    ctx->n_marks = 0;
+  } else if (enable && !ctx->prof) {
     for (int i = 0; i < 64; ++i) {
       if (cudaEventCreate(&ctx->marks[i]) != cudaSuccess) {
         cudaGetLastError();
@@ -276,7 +285,6 @@ int mla_profile_read(mla_ctx* ctx, float* ms, const char** names, int max_kernel
   int n = 0;
   if (ctx->n_marks > 0 && cudaEventSynchronize(ctx->marks[ctx->n_marks - 1]) != cudaSuccess) {
     cudaGetLastError();
-    ctx->n_marks = 0;
     return -1;
   }
   for (int i = 0; i + 1 < ctx->n_marks && n < max_kernels; ++i) {
@@ -290,7 +298,6 @@ int mla_profile_read(mla_ctx* ctx, float* ms, const char** names, int max_kernel
     names[n] = ctx->mark_names[i];
     ++n;
   }
-  ctx->n_marks = 0;
   return n;
 }
 

@@ -5,23 +5,28 @@
 // the query image Q = [W^UK_i^T q^C_i ; RoPE(q^R_i)] (128 heads x 576) and
 // the cached rows C = [c^KV ; k^R] (tokens x 576),
 //     s = Q C^T * scale,  a = softmax(s),  o_lat = a C[:, :512].
-// The 128 heads are the M = 128 side of both MMAs:
-//     S  (128 x 32 tokens)  = Q (128 x 576) . C_tile^T        -> TMEM, fp32
-//     O  (128 x 256 cols)  += P (128 x 32, bf16) . C_tile[:, half]
+// The 128 heads are the M = 128 side of both MMAs, 128 cache tokens the N
+// side of the score MMA (one tcgen05.mma takes about as long at N = 16 as at
+// N = 128, so narrow token tiles waste the tensor core):
+//     S (128 x 128 tokens)  = sum over 9 feature blocks Q_b . C_b^T  -> TMEM
+//     O (128 x 256 cols)   += P (128 x 128, bf16) . C[:, half]       -> TMEM
 // One CTA owns one KV split of one query token and one half (256 columns)
-// of the latent output; the two halves recompute the same S (so their
-// softmax statistics agree bit for bit) and keep their O half resident in
-// TMEM (256 + 2 x 32 of the 512 columns).
+// of the latent output; both halves compute the same S, so their softmax
+// statistics agree bit for bit.  TMEM: O half (256 columns) + two S buffers
+// (2 x 128), so S of the next tile is computed while the softmax of this one
+// runs.  Shared memory: the query image stays resident (144 KB); the cache
+// streams through a 3-deep ring of 16 KB stages, first as score blocks
+// [128 tokens x 64 features] (one per feature block), then as value slabs
+// [32 tokens x 256 features of this half].
 //
-// Roles (192 threads): warp 0 = TMA producer (query image by bulk copy once
-// per segment, 32-token cache tiles by tiled TMA into two 128B-swizzled
-// stages), warp 1 = MMA issuer + TMEM owner, warps 2-5 = softmax (thread =
-// head): online softmax in the log2 domain with a lazy rescale (O and l are
-// rescaled only when a row maximum grows by more than 2^8, so P <= 256),
-// P written to shared memory in the 64-byte swizzled K-major layout.  At the
-// end of a segment the same warps write O / l and m + log2 l for the
-// log-sum-exp combine.  Every wait is bounded; on a timeout the CTA records
-// MLA_ERR_TIMEOUT, drains its own loads and frees TMEM.
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM
+// owner, warps 2-5 = softmax (thread = head): online softmax in the log2
+// domain with a lazy rescale (O and l are rescaled only when a row maximum
+// grows by more than 2^8, so P <= 256), P written to shared memory in the
+// 128-byte swizzled K-major layout.  At the end of a segment the same warps
+// write O / l and m + log2 l for the log-sum-exp combine.  Every wait is
+// bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains its own
+// loads and frees TMEM.
 #include "layouts.cuh"
 #include "tc_util.cuh"
 #include "mla_internal.h"
@@ -30,17 +35,17 @@
 namespace mla {
 namespace {
 
-constexpr int kTok = 32;                                   // tokens per tile
-constexpr uint32_t kTileBlock = kTok * 128;                // one 64-feature box
-constexpr uint32_t kTileBytes = 9 * kTileBlock;            // 36864
-constexpr uint32_t kPBytes = 128 * kTok * 2;               // 8192
+constexpr int kTile = 128;                                 // tokens per tile (2 pages)
+constexpr int kRing = 3;                                   // ring stages
+constexpr uint32_t kStage = 16384;                         // one ring stage
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffTile = kQImgBytes;                  // 147456
-constexpr uint32_t kOffP = kOffTile + 2 * kTileBytes;      // 221184
+constexpr uint32_t kOffRing = kQImgBytes;                  // 147456
+constexpr uint32_t kOffP = kOffRing + kRing * kStage;      // 196608
+constexpr uint32_t kPBytes = 128 * kTile * 2;              // 32768
 constexpr uint32_t kOffBar = kOffP + kPBytes;              // 229376
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;                            // S buffers at 256, 288
+constexpr uint32_t kColS = 256;                            // S buffers at 256 and 384
 constexpr float kRescale = 8.0f;                           // log2 units
 
 struct AttArgs {
@@ -90,54 +95,53 @@ struct SegIter {
 };
 
 __device__ __forceinline__ int ntiles_of(int p0, int p1) {
-  return p1 > p0 ? (p1 - p0 + kTok - 1) / kTok : 0;
+  return p1 > p0 ? (p1 - p0 + kTile - 1) / kTile : 0;
 }
 
-__device__ __forceinline__ uint32_t p_off(int r, int chunk) {
-  // 64-byte swizzle: 8-row x 64 B atoms, chunk j of row r at j ^ ((r % 8) >> 1)
-  return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((chunk ^ ((r & 7) >> 1)) << 4));
+// value slabs (32 tokens) of tile i that hold at least one visible token
+__device__ __forceinline__ int nslabs_of(int tile_start, int p1) {
+  const int v = p1 - tile_start;
+  return v >= kTile ? 4 : (v + 31) / 32;
 }
 
-__device__ __forceinline__ uint64_t sdesc64(uint32_t saddr, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;                       // leading byte offset (unused): 16 B
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)4 << 61;                       // swizzle mode: 64-byte
-  return d;
+// P [128 heads][128 tokens] bf16, K-major, 128-byte swizzle: two 64-token
+// blocks of [128 rows][128 B]; 16-byte chunk c of row r (tokens 8c..8c+7).
+__device__ __forceinline__ uint32_t p_off(int r, int c) {
+  return (uint32_t)((c >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
+                    (((c & 7) ^ (r & 7)) << 4));
 }
 
 __global__ void __launch_bounds__(192, 1)
-attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
+attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
+                 const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bar;          // [2]
-  uint64_t* empty = bar + 2;     // [2]
-  uint64_t* s_full = bar + 4;    // [2]
-  uint64_t* q_full = bar + 6;
-  uint64_t* q_empty = bar + 7;
-  uint64_t* p_full = bar + 8;
-  uint64_t* pv_done = bar + 9;
-  uint64_t* o_free = bar + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 11);
+  uint64_t* full = bar;          // [kRing]
+  uint64_t* empty = bar + 4;     // [kRing]
+  uint64_t* s_full = bar + 8;    // [2] S buffer g&1 holds S(g)
+  uint64_t* p_full = bar + 10;   // P(g) written
+  uint64_t* pv_done = bar + 11;  // PV(g) done
+  uint64_t* q_full = bar + 12;
+  uint64_t* q_empty = bar + 13;
+  uint64_t* o_free = bar + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, t = blockIdx.y, half = blockIdx.z;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRing; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&s_full[i], 1);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(p_full, 128);
     mbar_init(pv_done, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     mbar_init(o_free, 128);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -146,7 +150,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
     tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmC);
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tmS);
+    tc::prefetch_tmap(&tmV);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -154,91 +161,158 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
   tc::grid_dep_wait();   // plan, query image and cache come from earlier kernels
 
   const uint32_t sQ = smem_u32(smem + kOffQ);
-  const uint32_t sT = smem_u32(smem + kOffTile);
+  const uint32_t sR = smem_u32(smem + kOffRing);
   const uint32_t sP = smem_u32(smem + kOffP);
-  int issued = 0;   // producer: cache tiles issued
+  const int oob_row = a.num_pages * kPage + kPage;   // TMA zero-fills rows out of range
+  int issued = 0;   // producer: ring stages issued
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      SegIter it;
-      it.init(&a, c, t);
-      int sb, p0, p1, slot, k = 0, g = 0;
-      while (it.next(&sb, &p0, &p1, &slot)) {
-        const int n = ntiles_of(p0, p1);
-        if (n == 0) continue;
-        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status, 21)) { *abort_flag = 1; break; }
-        if (*abort_flag) break;
-        tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
-        const uint8_t* qsrc = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes;
-        for (int fb = 0; fb < 9; ++fb)
-          tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
-        for (int i = 0; i < n; ++i, ++g) {
-          const int s = g & 1;
-          if (g >= 2 && !mbar_wait(&empty[s], ((g >> 1) - 1) & 1, a.status, 22)) {
-            *abort_flag = 1;
-            break;
-          }
-          if (*abort_flag) break;
-          const int p = p0 + i * kTok;
-          int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
-          if (pg < 0 || pg >= a.num_pages) {
-            report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
-            pg = 0;
-          }
-          const int y = pg * kPage + (p % kPage);
-          tc::mbar_arrive_expect_tx(smem_u32(&full[s]), kTileBytes);
-          for (int fb = 0; fb < 9; ++fb)
-            tc::tma_load_2d(sT + s * kTileBytes + fb * kTileBlock, &tmC, fb * 64, y,
-                            smem_u32(&full[s]));
-          issued = g + 1;
+      int rc = 0;
+      auto acquire = [&]() -> int {
+        const int s = rc % kRing;
+        if (rc >= kRing && !mbar_wait(&empty[s], ((rc / kRing) - 1) & 1, a.status, 22)) {
+          *abort_flag = 1;
+          return -1;
         }
-        if (*abort_flag) break;
-        ++k;
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idS = tc::idesc_bf16(128, kTok, false, false);
-      constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
-      SegIter it;
-      it.init(&a, c, t);
-      int sb, p0, p1, slot, k = 0, g = 0;
-      auto issue_s = [&](int gg) -> bool {
-        const int s = gg & 1;
-        if (!mbar_wait(&full[s], (gg >> 1) & 1, a.status, 23)) return false;
-        tc::fence_after_sync();
-        const uint32_t tile = sT + s * kTileBytes;
-#pragma unroll 4
-        for (int kk = 0; kk < 36; ++kk) {
-          const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t toff = (kk >> 2) * kTileBlock + (kk & 3) * 32;
-          tc::mma_ss(tmem + kColS + s * kTok, tc::sdesc(sQ + koff, 16, 1024),
-                     tc::sdesc(tile + toff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        if (*abort_flag) return -1;
+        tc::mbar_arrive_expect_tx(smem_u32(&full[s]), kStage);
+        ++rc;
+        issued = rc;
+        return s;
+      };
+      auto page_row = [&](int sb, int p) -> int {
+        int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
+        if (pg < 0 || pg >= a.num_pages) {
+          report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
+          pg = 0;
         }
-        tc::mma_commit(smem_u32(&s_full[s]));
+        return pg * kPage;
+      };
+      auto load_scores = [&](int sb, int ts, int p1) -> bool {
+        const int y0 = page_row(sb, ts);
+        const int y1 = ts + kPage < p1 ? page_row(sb, ts + kPage) : oob_row;
+        for (int b = 0; b < 9; ++b) {
+          const int s = acquire();
+          if (s < 0) return false;
+          const uint32_t dst = sR + s * kStage;
+          tc::tma_load_2d(dst, &tmS, b * 64, y0, smem_u32(&full[s]));
+          tc::tma_load_2d(dst + 8192, &tmS, b * 64, y1, smem_u32(&full[s]));
+        }
         return true;
       };
+      auto load_values = [&](int sb, int ts, int p1) -> bool {
+        const int ns = nslabs_of(ts, p1);
+        for (int v = 0; v < ns; ++v) {
+          const int s = acquire();
+          if (s < 0) return false;
+          const int p = ts + 32 * v;
+          const int y = page_row(sb, p) + (p % kPage);
+          const uint32_t dst = sR + s * kStage;
+          for (int f = 0; f < 4; ++f)
+            tc::tma_load_2d(dst + f * 4096, &tmV, half * 256 + f * 64, y, smem_u32(&full[s]));
+        }
+        return true;
+      };
+      SegIter it;
+      it.init(&a, c, t);
+      int sb, p0, p1, slot, k = 0;
       bool ok = true;
       while (ok && it.next(&sb, &p0, &p1, &slot)) {
         const int n = ntiles_of(p0, p1);
         if (n == 0) continue;
+        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status, 21)) { ok = false; break; }
+        if (*abort_flag) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
+        const uint8_t* qsrc = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes;
+        for (int fb = 0; fb < 9; ++fb)
+          tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
+        ok = load_scores(sb, p0, p1);
+        for (int i = 0; ok && i < n; ++i) {
+          if (i + 1 < n) ok = load_scores(sb, p0 + (i + 1) * kTile, p1);
+          if (ok) ok = load_values(sb, p0 + i * kTile, p1);
+        }
+        ++k;
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idS = tc::idesc_bf16(128, kTile, false, false);
+      constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
+      // descriptors at offset 0; a K step adds (byte offset / 16)
+      const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
+      const uint64_t dR = tc::sdesc(sR, 16, 1024);
+      const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
+      const uint64_t dP = tc::sdesc(sP, 16, 1024);
+      int rc = 0, g = 0, k = 0;
+      bool ok = true;
+      auto take = [&]() -> int {
+        const int s = rc % kRing;
+        if (!mbar_wait(&full[s], (rc / kRing) & 1, a.status, 23)) return -1;
+        tc::fence_after_sync();
+        ++rc;
+        return s;
+      };
+      auto issue_scores = [&](int gg) -> bool {
+        const uint32_t dcol = tmem + kColS + (gg & 1) * kTile;
+        for (int b = 0; b < 9; ++b) {
+          const int s = take();
+          if (s < 0) return false;
+          const uint64_t dRs = dR + ((s * kStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_ss(dcol, dQ + ((b * 16384 + kk * 32) >> 4), dRs + ((kk * 32) >> 4), idS,
+                       (b > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(smem_u32(&empty[s]));
+        }
+        tc::mma_commit(smem_u32(&s_full[gg & 1]));
+        return true;
+      };
+      SegIter it;
+      it.init(&a, c, t);
+      int sb, p0, p1, slot;
+      while (ok && it.next(&sb, &p0, &p1, &slot)) {
+        const int n = ntiles_of(p0, p1);
+        if (n == 0) continue;
         if (!mbar_wait(q_full, k & 1, a.status, 24)) { ok = false; break; }
+        if (!(ok = issue_scores(g))) break;
         for (int i = 0; i < n; ++i, ++g) {
-          if (i == 0 && !(ok = issue_s(g))) break;
-          if (i + 1 < n && !(ok = issue_s(g + 1))) break;
+          if (i + 1 < n && !(ok = issue_scores(g + 1))) break;
           if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
           if (i == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, a.status, 25))) break;
           if (!(ok = mbar_wait(p_full, g & 1, a.status, 26))) break;
           if (*abort_flag) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t tile = sT + (g & 1) * kTileBytes + half * 4 * kTileBlock;
+          const int ts = p0 + i * kTile;
+          const int ns = nslabs_of(ts, p1);
+          for (int v = 0; v < ns; ++v) {
+            const int s = take();
+            if (s < 0) { ok = false; break; }
+            const int vis = p1 - (ts + 32 * v);
+            if (vis < 32) {
+              // rows past the visible end hold stale pool data: zero them so
+              // that 0 * (Inf or NaN) cannot reach the accumulator
+              uint8_t* st0 = smem + kOffRing + s * kStage;
+              for (int e = vis * 32; e < 32 * 32; ++e) {
+                const int r = e >> 5, f = (e >> 3) & 3, ch = e & 7;
+                *reinterpret_cast<uint4*>(st0 + f * 4096 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+              }
+              tc::fence_async_smem();
+            }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            tc::mma_ss(tmem, sdesc64(sP + kk * 32, 512), tc::sdesc(tile + kk * 2048, kTileBlock, 1024),
-                       idO, (i > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&empty[g & 1]));
+            for (int kk = 0; kk < 2; ++kk) {
+              const int tk = 32 * v + 16 * kk;
+              tc::mma_ss(tmem, dP + (((tk >> 6) * 16384 + (tk & 63) * 2) >> 4),
+                         dV + ((s * kStage + kk * 2048) >> 4), idO,
+                         (i > 0 || v > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(smem_u32(&empty[s]));
+          }
+          if (!ok) break;
           tc::mma_commit(smem_u32(pv_done));
         }
         ++k;
@@ -250,6 +324,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;          // head
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    uint8_t* ps = smem + kOffP;
     SegIter it;
     it.init(&a, c, t);
     int sb, p0, p1, slot, g = 0;
@@ -266,28 +341,23 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
       }
       float m_used = -INFINITY, l = 0.f;
       for (int i = 0; i < n; ++i, ++g) {
-        const int s = g & 1;
-        ok = mbar_wait(&s_full[s], (g >> 1) & 1, a.status, 27);
+        const uint32_t scol = trow + kColS + (g & 1) * kTile;
+        ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, a.status, 27);
         if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
-        float x[32];
-        {
-          float v[16];
-          tc::tmem_ld16(trow + kColS + s * kTok, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = v[j];
-          tc::tmem_ld16(trow + kColS + s * kTok + 16, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x[16 + j] = v[j];
-        }
-        const int valid = min(kTok, p1 - (p0 + i * kTok));
+        const int valid = min(kTile, p1 - (p0 + i * kTile));
+        // pass 1: row maximum over the visible tokens of the tile
         float mx = -INFINITY;
+        for (int c0 = 0; c0 < kTile; c0 += 16) {
+          float x[16];
+          tc::tmem_ld16(scol + c0, x);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = j < valid ? x[j] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[j]);
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < valid) mx = fmaxf(mx, x[j]);
         }
+        mx *= a.scale_log2;
         if (i > 0) {
+          // P buffer reuse and a possible O rescale both need PV(g-1) done
           ok = mbar_wait(pv_done, (g - 1) & 1, a.status, 28);
           if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
           tc::fence_after_sync();
@@ -308,32 +378,26 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
           }
           m_used = m_new;
         }
+        // pass 2: P = 2^(s*scale - m) as bf16 into shared memory
         float psum = 0.f;
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < kTile; c0 += 16) {
+          float x[16];
+          tc::tmem_ld16(scol + c0, x);
+          uint32_t pk[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float e0 = exp2f(x[2 * j] - m_used), e1 = exp2f(x[2 * j + 1] - m_used);
-          psum += e0 + e1;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-          pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int j = 0; j < 8; ++j) {
+            const float e0 = c0 + 2 * j < valid ? exp2f(fmaf(x[2 * j], a.scale_log2, -m_used)) : 0.f;
+            const float e1 =
+                c0 + 2 * j + 1 < valid ? exp2f(fmaf(x[2 * j + 1], a.scale_log2, -m_used)) : 0.f;
+            psum += e0 + e1;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+            pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(ps + p_off(row, c0 >> 3)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(ps + p_off(row, (c0 >> 3) + 1)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
         l += psum;
-        if (valid < kTok) {
-          // rows past the visible end hold stale pool data: zero this half's
-          // columns of them so that 0 * (Inf or NaN) cannot reach the PV MMA
-          uint8_t* st0 = smem + kOffTile + s * kTileBytes + half * 4 * kTileBlock;
-          const int ntail = (kTok - valid) * 4 * 8;
-          for (int e = threadIdx.x - 64; e < ntail; e += 128) {
-            const int r = valid + (e >> 5), blk = (e >> 3) & 3, ch = e & 7;
-            *reinterpret_cast<uint4*>(st0 + blk * kTileBlock + (r >> 3) * 1024 + (r & 7) * 128 +
-                                      ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        uint8_t* prow_s = smem + kOffP;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-          *reinterpret_cast<uint4*>(prow_s + p_off(row, ch)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
         tc::fence_async_smem();
         tc::fence_before_sync();
         tc::mbar_arrive(smem_u32(p_full));
@@ -363,9 +427,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) {
-    for (int i = 0; i < 2 && i < issued; ++i) {
-      const int gl = issued - 1 - i;
-      mbar_wait(&full[gl & 1], (gl >> 1) & 1, a.status, 30, 1 << 20, 100000000ull);
+    for (int i = 0; i < kRing && i < issued; ++i) {
+      const int u = issued - 1 - i;
+      mbar_wait(&full[u % kRing], (u / kRing) & 1, a.status, 30, 1 << 20, 100000000ull);
     }
     mbar_wait(q_full, 0, a.status, 31, 1 << 20, 100000000ull);
   }
@@ -381,8 +445,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmC, const AttArgs a) {
 bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
                int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
                const WsLayout& L, cudaStream_t st) {
-  CUtensorMap tmC;
-  if (!make_tmap_bf16_2d(&tmC, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, kTok, false))
+  CUtensorMap tmS, tmV;
+  if (!make_tmap_bf16_2d(&tmS, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 64, false) ||
+      !make_tmap_bf16_2d(&tmV, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 32, false))
     return false;
   AttArgs a{};
   a.lens = reinterpret_cast<const int*>(ws + L.lens);
@@ -419,7 +484,7 @@ bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
   cfg.numAttrs = 1;
   prof_mark(ctx, st, "attend");
   ctx->launches += 1;
-  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tmC, a) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tmS, tmV, a) == cudaSuccess;
 }
 
 }  // namespace mla

@@ -16,53 +16,52 @@ namespace {
 
 // Merge the split partials of one (token, head) into o_lat = sum_s w_s O_s /
 // sum_s w_s with w_s = 2^(lse_s - max lse): the log-sum-exp combine of
-// flash-decoding.  One warp per (token, head); lane owns 16 latent columns.
+// flash-decoding.  One thread per (token, head, 4 latent columns); the
+// partial rows are read as coalesced float4 runs.
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                const int* __restrict__ slot_base, int T, int M,
                __nv_bfloat16* __restrict__ o_lat) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (gw >= M * kHeads) return;
-  const int m = gw / kHeads, head = gw % kHeads;
+  const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= M * kHeads * (kLat / 4)) return;
+  const int q4 = gid % (kLat / 4), mh = gid / (kLat / 4);
+  const int m = mh / kHeads, head = mh % kHeads;
   const int b = m / T, t = m % T;
   const int s0 = slot_base[b], s1 = slot_base[b + 1];
   float lmax = -INFINITY;
   for (int s = s0; s < s1; ++s) lmax = fmaxf(lmax, part_lse[((size_t)s * T + t) * kHeads + head]);
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
+#pragma unroll 4
   for (int s = s0; s < s1; ++s) {
     const size_t r = ((size_t)s * T + t) * kHeads + head;
     const float w = exp2f(part_lse[r] - lmax);
-    if (w == 0.f) continue;
     wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(part_o + r * kLat) + lane * 4;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 x = src[k];
-      acc[4 * k] = fmaf(w, x.x, acc[4 * k]);
-      acc[4 * k + 1] = fmaf(w, x.y, acc[4 * k + 1]);
-      acc[4 * k + 2] = fmaf(w, x.z, acc[4 * k + 2]);
-      acc[4 * k + 3] = fmaf(w, x.w, acc[4 * k + 3]);
-    }
+    if (w == 0.f) continue;
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(part_o + r * kLat) + q4);
+    acc.x = fmaf(w, x.x, acc.x);
+    acc.y = fmaf(w, x.y, acc.y);
+    acc.z = fmaf(w, x.z, acc.z);
+    acc.w = fmaf(w, x.w, acc.w);
   }
   const float inv = 1.f / wsum;
-  __align__(16) __nv_bfloat16 outv[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) outv[k] = __float2bfloat16_rn(acc[k] * inv);
-  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)m * kHeads + head) * kLat + lane * 16);
-  dst[0] = reinterpret_cast<const uint4*>(outv)[0];
-  dst[1] = reinterpret_cast<const uint4*>(outv)[1];
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&lo);
+  v.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(o_lat + (size_t)mh * kLat + q4 * 4) = v;
 }
 
 // K splits so that one wave fills the SMs, within the scratch budget.
+// Each split streams at least kMinChunks x 64 columns of its weight rows, so
+// that the fp32 partials stay small next to the weights they summarise.
 int choose_k_splits(const mla_ctx* ctx, int m_tiles, int n_tiles, int nt, int k_chunks,
-                    size_t partial_cap) {
+                    size_t partial_cap, int min_chunks = 4) {
   const int target = ctx->num_sms * wgemm_ctas_per_sm(nt);
   int s = target / std::max(1, m_tiles * n_tiles);
-  s = std::max(1, std::min(s, k_chunks));
+  s = std::max(1, std::min(s, k_chunks / min_chunks));
   while (s > 1 && (size_t)m_tiles * n_tiles * s * nt * 128 * sizeof(float) > partial_cap) --s;
   return s;
 }
@@ -158,7 +157,7 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
   a = base_args(ctx);
   a.n_tokens = M;
   a.k_chunks = D / 64;
-  a.splits = choose_k_splits(ctx, p.m_tiles * 1, p.n_tiles, p.nt, a.k_chunks, kAppendPartialBytes);
+  a.splits = choose_k_splits(ctx, p.m_tiles, p.n_tiles, p.nt, a.k_chunks, kAppendPartialBytes, 8);
   a.tiles_per_head = 5;
   a.a_tiles_main = 4;
   a.valid_rows_last = kRope;
@@ -221,7 +220,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     prof_mark(ctx, st, "combine");
     ctx->launches += 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((M * kHeads + 7) / 8);
+    cfg.gridDim = dim3((M * kHeads * (kLat / 4) + 255) / 256);
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

@@ -5,7 +5,9 @@
 // host never waits for it:
 //   * pages(b)      = ceil(len_b / page_size), len_b validated and clamped;
 //   * prefix[b]     = pages of sequences 0..b-1  (prefix[B] = P, all pages);
-//   * G_eff = min(G, P) splits are used, so none is empty; split c < G_eff
+//   * G_eff = min(G, max(1, P / kMinPagesPerSplit)) splits are used (none is
+//     empty, and short caches are not cut so thin that merging the partial
+//     results costs more than the attention itself); split c < G_eff
 //     owns global pages [floor(cP/G_eff), floor((c+1)P/G_eff));
 //   * first_split[b] = split holding page prefix[b]; the splits touching
 //     sequence b are first_split[b] .. split(prefix[b+1]-1);
@@ -19,6 +21,7 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kMinPagesPerSplit = 4;
 
 __device__ __forceinline__ long long split_of_page(long long g, long long P, int G) {
   return ((g + 1) * G - 1) / P;
@@ -80,14 +83,16 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int page, int ma
     if (threadIdx.x == 0) carry += tot;
     __syncthreads();
   }
+  const long long P = carry;
+  long long g_want = P / kMinPagesPerSplit;
+  if (g_want < 1) g_want = 1;
+  const int G = g_want < G_max ? (int)g_want : G_max;
   if (threadIdx.x == 0) {
     prefix[B] = carry;
-    meta[0] = carry < G_max ? carry : G_max;
+    meta[0] = G;
     meta[1] = carry;
   }
   __syncthreads();
-  const long long P = carry;
-  const int G = P < G_max ? (int)P : G_max;
   // pass 2: splits per sequence and their slot bases
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();

@@ -193,9 +193,24 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       for (int c0 = 0; c0 < NT; c0 += 16) {
         float v[16];
         if (a.splits > 1) {
+          // sum the partials in split order; four splits in flight at a time
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          for (int zz = 0; zz < a.splits; ++zz) {
+          int zz = 0;
+          for (; zz + 4 <= a.splits; zz += 4) {
+            float w[4][16];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float* p = part + (size_t)(zz + u) * NT * 128 + c0 * 128 + row;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) w[u][j] = __ldcg(p + j * 128);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += w[u][j];
+          }
+          for (; zz < a.splits; ++zz) {
             const float* p = part + (size_t)zz * NT * 128 + c0 * 128 + row;
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(p + j * 128);
@@ -219,7 +234,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             }
           }
         }
-        if (EPI == WG_QIMG) {
+        if constexpr (EPI == WG_QIMG) {
           const int f = tile * 128 + row;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -229,8 +244,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                                            (size_t)t * kQImgBytes + qimg_off(head, f)) =
                   bf16_bits(v[j]);
           }
-          continue;
-        }
+        } else {
         // stage 16 tokens x 128 rows as bf16, then 16-byte stores per token row
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg[j * kStgPitch + row] = bf16_bits(v[j]);
@@ -261,6 +275,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           *reinterpret_cast<uint4*>(dst) = val;
         }
         tc::named_sync(1, 128);
+        }
       }
       if (EPI == WG_QIMG && tile == 0) {
         // rotated q^R of this head for the tile's tokens -> image features 512..575
