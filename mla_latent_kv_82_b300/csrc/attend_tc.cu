@@ -14,16 +14,16 @@
 // of the latent output; both halves compute the same S, so their softmax
 // statistics agree bit for bit.  TMEM: O half (256 columns) + two S buffers
 // (2 x 128), so S of the next tile is computed while the softmax of this one
-// runs.  Shared memory: the query image stays resident (144 KB); the cache
-// streams through a 3-deep ring of 16 KB stages, first as score blocks
-// [128 tokens x 64 features] (one per feature block), then as value slabs
-// [32 tokens x 256 features of this half].
+// runs; P (bf16) overwrites the S buffer it came from and feeds the value
+// MMA straight from TMEM.  Shared memory: the query image stays resident
+// (144 KB); the cache streams through a 5-deep ring of 16 KB stages, first
+// as score blocks [128 tokens x 64 features] (one per feature block), then
+// as value slabs [32 tokens x 256 features of this half].
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM
 // owner, warps 2-5 = softmax (thread = head): online softmax in the log2
 // domain with a lazy rescale (O and l are rescaled only when a row maximum
-// grows by more than 2^8, so P <= 256), P written to shared memory in the
-// 128-byte swizzled K-major layout.  At the end of a segment the same warps
+// grows by more than 2^8, so P <= 256), P packed two bf16 per TMEM column.  At the end of a segment the same warps
 // write O / l and m + log2 l for the log-sum-exp combine.  Every wait is
 // bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains its own
 // loads and frees TMEM.
@@ -36,17 +36,16 @@ namespace mla {
 namespace {
 
 constexpr int kTile = 128;                                 // tokens per tile (2 pages)
-constexpr int kRing = 3;                                   // ring stages
+constexpr int kRing = 5;                                   // ring stages
 constexpr uint32_t kStage = 16384;                         // one ring stage
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = kQImgBytes;                  // 147456
-constexpr uint32_t kOffP = kOffRing + kRing * kStage;      // 196608
-constexpr uint32_t kPBytes = 128 * kTile * 2;              // 32768
-constexpr uint32_t kOffBar = kOffP + kPBytes;              // 229376
+constexpr uint32_t kOffBar = kOffRing + kRing * kStage;    // 229376
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;                            // S buffers at 256 and 384
 constexpr float kRescale = 8.0f;                           // log2 units
+constexpr int kPrefetchTiles = 3;                          // L2 prefetch distance
 
 struct AttArgs {
   const int* lens;
@@ -56,6 +55,7 @@ struct AttArgs {
   const int* meta;
   const int32_t* bt;
   const uint8_t* qimg;
+  const __nv_bfloat16* cache;
   float* part_o;
   float* part_lse;
   int* status;
@@ -104,13 +104,6 @@ __device__ __forceinline__ int nslabs_of(int tile_start, int p1) {
   return v >= kTile ? 4 : (v + 31) / 32;
 }
 
-// P [128 heads][128 tokens] bf16, K-major, 128-byte swizzle: two 64-token
-// blocks of [128 rows][128 B]; 16-byte chunk c of row r (tokens 8c..8c+7).
-__device__ __forceinline__ uint32_t p_off(int r, int c) {
-  return (uint32_t)((c >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 +
-                    (((c & 7) ^ (r & 7)) << 4));
-}
-
 __global__ void __launch_bounds__(192, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
                  const AttArgs a) {
@@ -119,14 +112,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                                              ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* full = bar;          // [kRing]
-  uint64_t* empty = bar + 4;     // [kRing]
-  uint64_t* s_full = bar + 8;    // [2] S buffer g&1 holds S(g)
-  uint64_t* p_full = bar + 10;   // P(g) written
-  uint64_t* pv_done = bar + 11;  // PV(g) done
-  uint64_t* q_full = bar + 12;
-  uint64_t* q_empty = bar + 13;
-  uint64_t* o_free = bar + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* empty = bar + 8;     // [kRing]
+  uint64_t* s_full = bar + 16;   // [2] S buffer g&1 holds S(g)
+  uint64_t* p_full = bar + 18;   // P(g) written
+  uint64_t* pv_done = bar + 19;  // PV(g) done
+  uint64_t* q_full = bar + 20;
+  uint64_t* q_empty = bar + 21;
+  uint64_t* o_free = bar + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,7 +155,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
 
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sR = smem_u32(smem + kOffRing);
-  const uint32_t sP = smem_u32(smem + kOffP);
   const int oob_row = a.num_pages * kPage + kPage;   // TMA zero-fills rows out of range
   int issued = 0;   // producer: ring stages issued
 
@@ -202,6 +194,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         }
         return true;
       };
+      // pages of the tile starting at ts into L2, so the ring's TMA loads hit
+      // L2 instead of waiting on HBM (each page is 64 x 1152 contiguous bytes)
+      auto prefetch_tile = [&](int sb, int ts, int p1) {
+        for (int pp = 0; pp < 2 && ts + pp * kPage < p1; ++pp) {
+          const int pg = a.bt[(size_t)sb * a.max_pages + (ts + pp * kPage) / kPage];
+          if (pg >= 0 && pg < a.num_pages)
+            tc::prefetch_l2(a.cache + (size_t)pg * kPage * kRow, kPage * kRow * 2);
+        }
+      };
       auto load_values = [&](int sb, int ts, int p1) -> bool {
         const int ns = nslabs_of(ts, p1);
         for (int v = 0; v < ns; ++v) {
@@ -228,8 +229,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         const uint8_t* qsrc = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes;
         for (int fb = 0; fb < 9; ++fb)
           tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
+        for (int i = 0; i < n && i < kPrefetchTiles; ++i) prefetch_tile(sb, p0 + i * kTile, p1);
         ok = load_scores(sb, p0, p1);
         for (int i = 0; ok && i < n; ++i) {
+          if (i + kPrefetchTiles < n) prefetch_tile(sb, p0 + (i + kPrefetchTiles) * kTile, p1);
           if (i + 1 < n) ok = load_scores(sb, p0 + (i + 1) * kTile, p1);
           if (ok) ok = load_values(sb, p0 + i * kTile, p1);
         }
@@ -246,9 +249,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
       const uint64_t dR = tc::sdesc(sR, 16, 1024);
       const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
-      const uint64_t dP = tc::sdesc(sP, 16, 1024);
-      int rc = 0, g = 0, k = 0;
+      int rc = 0, g = 0, k = 0, pv_issued = 0, pv_seen = 0;
       bool ok = true;
+      // S(x) overwrites the buffer that held P(x-2): wait until every issued
+      // value MMA has finished.  At most one is ever outstanding, so each
+      // parity wait below targets the barrier's current or next phase.
+      auto drain_pv = [&]() -> bool {
+        while (pv_seen < pv_issued) {
+          if (!mbar_wait(pv_done, pv_seen & 1, a.status, 33)) return false;
+          ++pv_seen;
+        }
+        return true;
+      };
       auto take = [&]() -> int {
         const int s = rc % kRing;
         if (!mbar_wait(&full[s], (rc / kRing) & 1, a.status, 23)) return -1;
@@ -278,14 +290,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         const int n = ntiles_of(p0, p1);
         if (n == 0) continue;
         if (!mbar_wait(q_full, k & 1, a.status, 24)) { ok = false; break; }
-        if (!(ok = issue_scores(g))) break;
+        if (!(ok = drain_pv()) || !(ok = issue_scores(g))) break;
         for (int i = 0; i < n; ++i, ++g) {
-          if (i + 1 < n && !(ok = issue_scores(g + 1))) break;
+          if (i + 1 < n && (!(ok = drain_pv()) || !(ok = issue_scores(g + 1)))) break;
           if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
           if (i == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, a.status, 25))) break;
           if (!(ok = mbar_wait(p_full, g & 1, a.status, 26))) break;
           if (*abort_flag) { ok = false; break; }
           tc::fence_after_sync();
+          // at most one value MMA in flight, so pv_done is never two phases ahead
+          if (!(ok = drain_pv())) break;
           const int ts = p0 + i * kTile;
           const int ns = nslabs_of(ts, p1);
           for (int v = 0; v < ns; ++v) {
@@ -305,8 +319,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             }
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const int tk = 32 * v + 16 * kk;
-              tc::mma_ss(tmem, dP + (((tk >> 6) * 16384 + (tk & 63) * 2) >> 4),
+              // P tokens 32v+16kk.. live in columns (32v+16kk)/2.. of S buffer g&1
+              tc::mma_ts(tmem, tmem + kColS + (g & 1) * kTile + 16 * v + 8 * kk,
                          dV + ((s * kStage + kk * 2048) >> 4), idO,
                          (i > 0 || v > 0 || kk > 0) ? 1u : 0u);
             }
@@ -314,6 +328,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           }
           if (!ok) break;
           tc::mma_commit(smem_u32(pv_done));
+          ++pv_issued;
         }
         ++k;
       }
@@ -324,7 +339,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;          // head
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* ps = smem + kOffP;
     SegIter it;
     it.init(&a, c, t);
     int sb, p0, p1, slot, g = 0;
@@ -378,14 +392,23 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           }
           m_used = m_new;
         }
-        // pass 2: P = 2^(s*scale - m) as bf16 into shared memory
+        // pass 2: P = 2^(s*scale - m) as bf16, written over the S columns
+        // already read (tokens c0..c0+31 -> columns c0/2..c0/2+15)
         float psum = 0.f;
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
-          float x[16];
-          tc::tmem_ld16(scol + c0, x);
-          uint32_t pk[8];
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          float x[32];
+          {
+            float v[16];
+            tc::tmem_ld16(scol + c0, v);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 16; ++j) x[j] = v[j];
+            tc::tmem_ld16(scol + c0 + 16, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[16 + j] = v[j];
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
             const float e0 = c0 + 2 * j < valid ? exp2f(fmaf(x[2 * j], a.scale_log2, -m_used)) : 0.f;
             const float e1 =
                 c0 + 2 * j + 1 < valid ? exp2f(fmaf(x[2 * j + 1], a.scale_log2, -m_used)) : 0.f;
@@ -393,12 +416,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
             pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(ps + p_off(row, c0 >> 3)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(ps + p_off(row, (c0 >> 3) + 1)) =
-              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          tc::tmem_st16_u32(scol + (c0 >> 1), pk);
         }
         l += psum;
-        tc::fence_async_smem();
         tc::fence_before_sync();
         tc::mbar_arrive(smem_u32(p_full));
       }
@@ -457,6 +477,7 @@ bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
   a.meta = reinterpret_cast<const int*>(ws + L.meta);
   a.bt = bt;
   a.qimg = reinterpret_cast<const uint8_t*>(qimg);
+  a.cache = cache;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   a.status = ctx->status;
