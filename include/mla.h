@@ -146,6 +146,29 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache,
                       const int32_t* seq_lens, int batch, int T, void* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode without a workspace argument, for callers that cannot allocate
+ * device memory when they decode (a fixed memory budget reserved up front,
+ * an allocator that is not reachable from the issuing thread, a plugin that
+ * is only handed its input and output buffers).  The pages have no
+ * counterpart to this call: it is a packaging of mla_decode.
+ *
+ * Same arguments, layouts and results as mla_decode, minus the workspace:
+ * the scratch is a 32 MiB array that the library reserves statically on
+ * every GPU where its device code is loaded (held until the process exits).
+ * The call itself allocates nothing.  Shapes whose
+ * mla_decode_workspace_size exceeds 32 MiB return MLA_ERR_WORKSPACE before
+ * anything is enqueued.  The first call on a device looks up the array's
+ * device address (once per device); make that first call before any stream
+ * capture.  All calls share the one array, so calls that overlap on the GPU
+ * (other streams, threads or contexts) race and give wrong results; nothing
+ * in it needs to be cleared between calls. */
+mla_status mla_decode_static_workspace(mla_ctx* ctx, const void* q,
+                                       const void* cache, int num_pages,
+                                       const int32_t* block_table,
+                                       int max_pages, const int32_t* seq_lens,
+                                       int batch, int T, void* out,
+                                       void* stream);
+
 /* Offsets (bytes from the workspace start) of two intermediates that
  * mla_decode leaves in the workspace, for diagnostics: the latent attention
  * output o_lat [batch*T, n_heads, d_latent] (sum_p a_p c_p) and the value

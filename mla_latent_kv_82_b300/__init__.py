@@ -29,6 +29,7 @@ EXPORTED = (
     "mla_create", "mla_destroy", "mla_compress_append", "mla_decode_workspace_size",
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
+    "mla_decode_static_workspace",
 )
 
 
@@ -74,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "mla_selftest_bounded_wait": ([vp, i32, vp], i32),
         "mla_status_string": ([i32], ctypes.c_char_p),
         "mla_profile_enable": ([vp, i32], i32),
+        "mla_decode_static_workspace": ([vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp], i32),
         "mla_profile_read": ([vp, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_char_p), i32], i32),
     }
@@ -124,6 +126,14 @@ def mla_decode(ctx, q, cache, num_pages, block_table, max_pages, seq_lens, batch
                workspace, workspace_bytes, stream) -> int:
     return _lib.mla_decode(ctx, q, cache, num_pages, block_table, max_pages, seq_lens, batch, T,
                            out, workspace, workspace_bytes, stream)
+
+
+def mla_decode_static_workspace(ctx, q, cache, num_pages, block_table, max_pages, seq_lens,
+                                batch, T, out, stream) -> int:
+    """mla_decode with the library's static scratch instead of a workspace
+    argument (for callers that cannot allocate device memory at decode time)."""
+    return _lib.mla_decode_static_workspace(ctx, q, cache, num_pages, block_table, max_pages,
+                                            seq_lens, batch, T, out, stream)
 
 
 def mla_decode_workspace_offsets(ctx, batch, T, max_pages) -> tuple[int, int, int]:
