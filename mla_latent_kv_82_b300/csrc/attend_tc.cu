@@ -125,6 +125,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x, t = blockIdx.y, half = blockIdx.z;
 
+  tc::grid_dep_launch();
+  tc::grid_dep_wait();   // plan, query image and cache come from earlier kernels
+  if (c >= a.meta[0]) return;   // more CTAs than KV splits in use
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&full[i], 1);
@@ -151,7 +155,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  tc::grid_dep_wait();   // plan, query image and cache come from earlier kernels
 
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sR = smem_u32(smem + kOffRing);

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                const int* __restrict__ slot_base, int T, int M,
                __nv_bfloat16* __restrict__ o_lat) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gid = blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= M * kHeads * (kLat / 4)) return;

@@ -21,7 +21,7 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kMinPagesPerSplit = 4;
+constexpr int kMinPagesPerSplit = 2;
 
 __device__ __forceinline__ long long split_of_page(long long g, long long P, int G) {
   return ((g + 1) * G - 1) / P;
@@ -60,6 +60,9 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int page, int ma
             int* slot_base, int* meta, int* status) {
   __shared__ int tmp[32];
   __shared__ int carry;
+  // seq_lens may have been written by the kernel before us
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   // pass 1: validated lengths and the page prefix
@@ -176,11 +179,21 @@ WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages) {
 
 void launch_plan(const mla_ctx* ctx, const WsLayout& L, char* ws, const int32_t* seq_lens,
                  int B, int T, int max_pages, cudaStream_t st) {
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(
-      seq_lens, B, T, ctx->cfg.page_size, max_pages, ctx->cfg.max_position, L.G,
-      reinterpret_cast<int*>(ws + L.lens), reinterpret_cast<int*>(ws + L.page_prefix),
-      reinterpret_cast<int*>(ws + L.first_split), reinterpret_cast<int*>(ws + L.slot_base),
-      reinterpret_cast<int*>(ws + L.meta), ctx->status);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, B, T, ctx->cfg.page_size, max_pages,
+                     ctx->cfg.max_position, L.G, reinterpret_cast<int*>(ws + L.lens),
+                     reinterpret_cast<int*>(ws + L.page_prefix),
+                     reinterpret_cast<int*>(ws + L.first_split),
+                     reinterpret_cast<int*>(ws + L.slot_base), reinterpret_cast<int*>(ws + L.meta),
+                     ctx->status);
 }
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st) {

@@ -86,6 +86,9 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   int issued = 0;
+  // let the next kernel's CTAs start their prologue and weight loads on free
+  // SMs; they still wait (griddepcontrol.wait) before touching our outputs
+  tc::grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {

@@ -1,7 +1,7 @@
 """Properties of the split-KV plan arithmetic (host logic, CPU only).
 
 The device planner cuts the concatenated page list of all sequences into
-G_eff = min(G, max(1, P // 4)) contiguous splits, split c owning [floor(cP/G_eff),
+G_eff = min(G, max(1, P // 2)) contiguous splits, split c owning [floor(cP/G_eff),
 floor((c+1)P/G_eff)), and gives split c's piece of sequence b the slot
 slot_base[b] + c - first_split[b].  These integer formulas are restated
 here and checked for coverage, balance, non-empty splits and slot bounds
@@ -15,7 +15,7 @@ def plan(lens, page, G_max):
     pages = [(L + page - 1) // page for L in lens]
     prefix = np.concatenate([[0], np.cumsum(pages)]).astype(np.int64)
     P = int(prefix[-1])
-    G = min(G_max, max(1, P // 4))
+    G = min(G_max, max(1, P // 2))
 
     def split_of(g):
         return ((g + 1) * G - 1) // P
@@ -67,7 +67,7 @@ def test_plan_covers_every_page_once_with_valid_slots(seed):
 
 def test_more_splits_than_pages_is_clamped():
     out, P, G, slot_base = pieces([1, 1, 1, 65, 200, 1000], 64, 74)
-    assert P == 25 and G == 6
+    assert P == 25 and G == 12
     assert slot_base[-1] <= G + 6 - 1
     out, P, G, slot_base = pieces([1], 64, 74)
     assert P == 1 and G == 1
