@@ -9,7 +9,7 @@ when the timed region starts; L2 is flushed (a 2x-L2 buffer is written,
 then another is read) before every timed step, outside the step's own
 CUDA-event bracket.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b1-l4096]
                   [--impl mla|reference]
 
 --impl reference times the fp64 CPU oracle (the reference of this build)
@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s and latent-cache GB/s (% of B300 roofline), 1 GPU"
-DEFAULT_STEPS = {"c1": 200, "c2": 1000, "c3": 300, "c4": 300, "c5": 50}
+DEFAULT_STEPS = {"tiny-fp32": 200, "b1-l4096": 1000, "b64-paged": 300, "b4-l128k": 300, "b128-l16k-t2": 50}
 
 
 # ----------------------------------------------------------------------------- setup
@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--config", default="b1-l4096",
+                    choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2"])
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -67,6 +68,30 @@ def load_peaks():
                 "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
             "source": "fallback"}
+
+
+def csrc_hash() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_82_b300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(config_key: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(config_key, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("csrc_sha256_16") != csrc_hash():
+        return None
+    return rec["dram_bytes"]
 
 
 # ----------------------------------------------------------------------------- work model
@@ -362,7 +387,7 @@ def run_mla(a, wl, rank, local_rank, world):
         roof = {"bound": "tensor", "achieved": f_dom / t_dom / 1e12, "peak": tf_peak,
                 "unit": "TFLOP/s"}
     roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": dom,
-                 "traffic": None, "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 "traffic": captured_traffic(a.config, dom), "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                  if peaks["source"] == "measured" else "fallback",
                  "algorithmic_bytes_per_launch": b_dom, "algorithmic_flops_per_launch": f_dom,
                  "avg_launch_ms": avg[dom],

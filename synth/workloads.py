@@ -5,7 +5,8 @@ seeded numbers go where, so that the CUDA library and the oracle see the
 same inputs.
 
 Widths follow the DeepSeek-V2 form of Multi-head Latent Attention as the
-pages give it (liang.world "DeepSeek-V2 architecture revolution", ch. 2:
+pages give it (page "DeepSeek-V2：在“大力出奇迹”的AI军备竞赛中，四两拨千斤",
+liang.world, 第二章:
 d = 5120, n_h = 128, d_h = 128, d_c = 512, d_h^R = 64); the tiny fp32 case
 uses n_h = 4, d_c = 32, d_R = 8, d_h = 16, d = 64.
 
@@ -142,23 +143,23 @@ class Workload:
                         self.torch_dtype, device=device)
 
 
-def c3_lens() -> list:
+def paged_lens() -> list:
     return [int(x) for x in np.random.default_rng(0).integers(1024, 8193, 64)]
 
 
 def config(name: str) -> Workload:
-    """The five named workloads, by the short names used in tests and bench."""
-    if name == "c1":   # tiny fp32 oracle check: 64 cached rows in total
+    """The five named workloads, by the short keys used in tests and bench."""
+    if name == "tiny-fp32":   # tiny fp32 oracle check: 64 cached rows in total
         return Workload("tiny-fp32-L64", TINY, "f32", [63], 1, False)
-    if name == "c2":   # batch 1, contiguous cache of 4096 tokens
+    if name == "b1-l4096":   # batch 1, contiguous cache of 4096 tokens
         return Workload("v2-b1-L4096-contig", V2, "bf16", [4095], 1, False)
-    if name == "c3":   # batch 64, lengths U[1024, 8192], shuffled pages
-        return Workload("v2-b64-paged-Lrand", V2, "bf16", c3_lens(), 1, True)
-    if name == "c4":   # batch 4, 128K cached tokens each
+    if name == "b64-paged":   # batch 64, lengths U[1024, 8192], shuffled pages
+        return Workload("v2-b64-paged-Lrand", V2, "bf16", paged_lens(), 1, True)
+    if name == "b4-l128k":   # batch 4, 128K cached tokens each
         return Workload("v2-b4-L131072", V2, "bf16", [131071] * 4, 1, False)
-    if name == "c5":   # batch 128, L=16384, two query tokens, full step
+    if name == "b128-l16k-t2":   # batch 128, L=16384, two query tokens, full step
         return Workload("v2-b128-L16384-T2", V2, "bf16", [16384] * 128, 2, False)
     raise KeyError(name)
 
 
-CONFIG_NAMES = ("c1", "c2", "c3", "c4", "c5")
+CONFIG_NAMES = ("tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2")

@@ -2,8 +2,9 @@
 
 Small cases span several 64-token tiles with ragged tails, single-slot
 sequences and T=2 with the causal mask across a page boundary; the five
-named workloads run at full size with every sequence (c1, c2) or a seeded
-sample of sequences (c3, c4, c5) compared with the oracle.
+named workloads run at full size with every sequence (tiny-fp32, b1-l4096)
+or a seeded sample of sequences (b64-paged, b128-l16k-t2, b4-l128k) compared
+with the oracle.
 """
 import numpy as np
 import pytest
@@ -75,8 +76,8 @@ def test_tiny_f32(T, lens, page):
     _compare_all(st, "explicit")
 
 
-def test_c1_tiny_config():
-    st = _run(W.config("c1"))
+def test_tiny_fp32_workload():
+    st = _run(W.config("tiny-fp32"))
     s = _compare_all(st, "explicit")
     assert s[0]["max_rel"] <= TOL["f32"][0]
 
@@ -163,15 +164,15 @@ def test_bounded_wait_gives_up_with_status():
 
 
 # --------------------------------------------------------------------------- full size
-def test_c2_full():
-    st = _run(W.config("c2"))
+def test_b1_l4096_full():
+    st = _run(W.config("b1-l4096"))
     _compare_all(st, "explicit")
 
 
 @pytest.mark.parametrize("name,seqs", [
-    ("c3", [0, 7, 21, 33, 40, 63]),
-    ("c5", [0, 127]),
-    ("c4", [3]),
+    ("b64-paged", [0, 7, 21, 33, 40, 63]),
+    ("b128-l16k-t2", [0, 127]),
+    ("b4-l128k", [3]),
 ])
 def test_full_configs_sampled(name, seqs):
     wl = W.config(name)

@@ -65,18 +65,18 @@ def test_fill_offsets_compose():
 
 
 def test_workload_recipes():
-    c3 = workloads.config("c3")
-    assert (c3.B, min(c3.lens), max(c3.lens), sum(c3.lens)) == (64, 1043, 8172, 299418)
-    assert c3.num_pages == 4709
-    bt = c3.block_table()
+    paged = workloads.config("b64-paged")
+    assert (paged.B, min(paged.lens), max(paged.lens), sum(paged.lens)) == (64, 1043, 8172, 299418)
+    assert paged.num_pages == 4709
+    bt = paged.block_table()
     used = bt[bt >= 0]
-    assert sorted(used.tolist()) == list(range(c3.num_pages))
-    c5 = workloads.config("c5")
-    assert c5.seq_lens[0] == 16386 and c5.T == 2
-    c2 = workloads.config("c2")
-    assert (c2.block_table()[0] == np.arange(64)).all()
-    assert workloads.config("c1").dims.softmax_scale == 1 / math.sqrt(24)
+    assert sorted(used.tolist()) == list(range(paged.num_pages))
+    t2 = workloads.config("b128-l16k-t2")
+    assert t2.seq_lens[0] == 16386 and t2.T == 2
+    b1 = workloads.config("b1-l4096")
+    assert (b1.block_table()[0] == np.arange(64)).all()
+    assert workloads.config("tiny-fp32").dims.softmax_scale == 1 / math.sqrt(24)
     assert workloads.V2.softmax_scale == 1 / math.sqrt(192)
     # h rows of a sequence are slices of one virtual tensor
-    h = c3.h_rows(2, 10, 12)
-    assert torch.equal(h[1], c3.h_rows(2, 11, 12)[0])
+    h = paged.h_rows(2, 10, 12)
+    assert torch.equal(h[1], paged.h_rows(2, 11, 12)[0])
