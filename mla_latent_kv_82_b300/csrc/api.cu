@@ -217,15 +217,16 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache, int num_pa
   if (!g.ok) return MLA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  mla::prof_mark(ctx, st, "plan");
-  mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
-  ctx->launches += 1;
   bool launched = true;
   if (ctx->cfg.dtype == MLA_BF16) {
     launched = mla::bf16_decode(ctx, static_cast<const __nv_bfloat16*>(q),
-                     static_cast<const __nv_bfloat16*>(cache), num_pages, block_table, max_pages,
-                     batch, T, static_cast<__nv_bfloat16*>(out), ws, L, st);
+                                static_cast<const __nv_bfloat16*>(cache), num_pages, block_table,
+                                max_pages, seq_lens, batch, T, static_cast<__nv_bfloat16*>(out),
+                                ws, L, st);
   } else {
+    mla::prof_mark(ctx, st, "plan");
+    mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
+    ctx->launches += 1;
     mla::f32_decode(ctx, static_cast<const float*>(q), static_cast<const float*>(cache),
                     num_pages, block_table, max_pages, batch, T, static_cast<float*>(out), ws,
                     L, st);

@@ -1,8 +1,9 @@
 // bf16 decode step at DeepSeek-V2 head widths: launches and small kernels.
 //
 //   append   : wgemm [W^DKV; W^KR] h  (+RoPE, paged 16-byte stores)
-//   decode   : plan -> wgemm absorb (query image) -> attend (split-KV)
-//              -> combine (o_lat, bf16) -> wgemm W^UV -> wgemm W_O
+//   decode   : wgemm absorb (query image; CTA 0 also builds the split plan)
+//              -> attend (split-KV) -> combine (o_lat, bf16) -> wgemm W^UV
+//              -> wgemm W_O
 // Every launch after the first of a call uses programmatic dependent launch.
 #include <algorithm>
 
@@ -39,7 +40,7 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
     const size_t r = ((size_t)s * T + t) * kHeads + head;
     const float w = exp2f(part_lse[r] - lmax);
     wsum += w;
-    if (w == 0.f) continue;
+    if (w == 0.f) continue;   // an empty split (no visible token) contributes nothing
     const float4 x = __ldcg(reinterpret_cast<const float4*>(part_o + r * kLat) + q4);
     acc.x = fmaf(w, x.x, acc.x);
     acc.y = fmaf(w, x.y, acc.y);
@@ -56,10 +57,13 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
 }
 
 // K splits so that one wave fills the SMs, within the scratch budget.
-// Each split streams at least kMinChunks x 64 columns of its weight rows, so
-// that the fp32 partials stay small next to the weights they summarise.
+// Each split streams at least min_chunks (and at least nt / 8) 64-column
+// chunks of its weight rows, so that its fp32 partial (nt x 128 x 4 bytes)
+// stays small next to the weights it summarises and the last CTA's
+// reduction stays short.
 int choose_k_splits(const mla_ctx* ctx, int m_tiles, int n_tiles, int nt, int k_chunks,
                     size_t partial_cap, int min_chunks = 4) {
+  min_chunks = std::max(min_chunks, nt / 8);
   const int target = ctx->num_sms * wgemm_ctas_per_sm(nt);
   int s = target / std::max(1, m_tiles * n_tiles);
   s = std::max(1, std::min(s, k_chunks / min_chunks));
@@ -67,23 +71,39 @@ int choose_k_splits(const mla_ctx* ctx, int m_tiles, int n_tiles, int nt, int k_
   return s;
 }
 
+// Token tile for a GEMM with m_tiles weight tiles: the smallest power of two
+// covering M (16..256), halved while fewer than 32 output tiles would exist,
+// so that GEMMs with few weight rows still spread over the SMs.
+int pick_token_tile(int M, int m_tiles) {
+  int nt = wgemm_token_tile(M);
+  while (nt > 16 && (long long)m_tiles * ((M + nt - 1) / nt) < 32) nt >>= 1;
+  return nt;
+}
+
+struct GemmShape {
+  int nt, n_tiles, splits;
+};
+
+GemmShape gemm_shape(const mla_ctx* ctx, int M, int m_tiles, int k_chunks, int min_chunks,
+                     size_t partial_cap) {
+  GemmShape g;
+  g.nt = pick_token_tile(M, m_tiles);
+  g.n_tiles = (M + g.nt - 1) / g.nt;
+  g.splits = choose_k_splits(ctx, m_tiles, g.n_tiles, g.nt, k_chunks, partial_cap, min_chunks);
+  return g;
+}
+
 struct Bf16Plans {
-  int nt, n_tiles;
-  int s_uv, s_o;
+  GemmShape abs, uv, o;
 };
 
 Bf16Plans decode_plans(const mla_ctx* ctx, int M) {
+  const size_t cap = 64u << 20;   // bound on the split-K scratch of the largest-M cases
   Bf16Plans p;
-  p.nt = wgemm_token_tile(M);
-  p.n_tiles = (M + p.nt - 1) / p.nt;
-  const size_t big = (size_t)1 << 40;
-  p.s_uv = choose_k_splits(ctx, kHeads, p.n_tiles, p.nt, kLat / 64, big);
-  p.s_o = choose_k_splits(ctx, ctx->cfg.d_model / 128, p.n_tiles, p.nt, kHeads * kDv / 64, big);
-  // keep the scratch of the largest-M cases bounded
-  const size_t cap = 64u << 20;
-  while (p.s_o > 1 && (size_t)(ctx->cfg.d_model / 128) * p.n_tiles * p.s_o * p.nt * 512 > cap)
-    --p.s_o;
-  while (p.s_uv > 1 && (size_t)kHeads * p.n_tiles * p.s_uv * p.nt * 512 > cap) --p.s_uv;
+  p.abs = gemm_shape(ctx, M, kHeads * (kLat / 128), kNope / 64, 4, 0);
+  p.abs.splits = 1;   // two K chunks only: never split
+  p.uv = gemm_shape(ctx, M, kHeads, kLat / 64, 4, cap);
+  p.o = gemm_shape(ctx, M, ctx->cfg.d_model / 128, kHeads * kDv / 64, 4, cap);
   return p;
 }
 
@@ -108,8 +128,8 @@ bool check(cudaError_t e) {
 
 size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M) {
   const Bf16Plans p = decode_plans(ctx, M);
-  const size_t uv = (size_t)kHeads * p.n_tiles * p.s_uv * p.nt * 128 * sizeof(float);
-  const size_t o = (size_t)(ctx->cfg.d_model / 128) * p.n_tiles * p.s_o * p.nt * 128 *
+  const size_t uv = (size_t)kHeads * p.uv.n_tiles * p.uv.splits * p.uv.nt * 128 * sizeof(float);
+  const size_t o = (size_t)(ctx->cfg.d_model / 128) * p.o.n_tiles * p.o.splits * p.o.nt * 128 *
                    sizeof(float);
   return std::max(uv, o);
 }
@@ -144,8 +164,9 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
   const int M = B * T, D = ctx->cfg.d_model;
   WgPlan p{};
-  p.nt = wgemm_token_tile(M);
-  p.n_tiles = (M + p.nt - 1) / p.nt;
+  const GemmShape g = gemm_shape(ctx, M, 5, D / 64, 8, kAppendPartialBytes);
+  p.nt = g.nt;
+  p.n_tiles = g.n_tiles;
   if (p.n_tiles > 65535) return false;
   p.m_tiles = 5;   // 4 tiles of W^DKV rows, 1 tile of W^KR rows
   p.tmA = ctx->tm_wdkv;
@@ -158,7 +179,7 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
   a = base_args(ctx);
   a.n_tokens = M;
   a.k_chunks = D / 64;
-  a.splits = choose_k_splits(ctx, p.m_tiles, p.n_tiles, p.nt, a.k_chunks, kAppendPartialBytes, 8);
+  a.splits = g.splits;
   a.tiles_per_head = 5;
   a.a_tiles_main = 4;
   a.valid_rows_last = kRope;
@@ -176,11 +197,12 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
 }
 
 bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
-                 int num_pages, const int32_t* bt, int max_pages, int B, int T,
-                 __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st) {
+                 int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
+                 int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
+                 cudaStream_t st) {
   const int M = B * T, D = ctx->cfg.d_model;
   const Bf16Plans bp = decode_plans(ctx, M);
-  if (bp.n_tiles > 65535) return false;
+  if (bp.abs.n_tiles > 65535 || bp.uv.n_tiles > 65535 || bp.o.n_tiles > 65535) return false;
   __nv_bfloat16* qimg = reinterpret_cast<__nv_bfloat16*>(ws + L.qfull);
   __nv_bfloat16* olat = reinterpret_cast<__nv_bfloat16*>(ws + L.o_lat);
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(ws + L.o);
@@ -189,8 +211,8 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   // ---- absorbed query: W^UK_i^T q^C_i (+ rotated q^R) -> query image
   {
     WgPlan p{};
-    p.nt = bp.nt;
-    p.n_tiles = bp.n_tiles;
+    p.nt = bp.abs.nt;
+    p.n_tiles = bp.abs.n_tiles;
     p.m_tiles = kHeads * (kLat / 128);
     p.tmA = ctx->tm_wuk;
     p.tmA2 = ctx->tm_wuk;
@@ -208,8 +230,14 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     a.b_head_cols = kNope + kRope;
     a.qimg = qimg;
     a.q = q;
-    a.lens = reinterpret_cast<const int*>(ws + L.lens);
     a.T = T;
+    a.do_plan = 1;
+    a.plan = PlanArgs{seq_lens, B, T, kPage, max_pages, ctx->cfg.max_position, L.G,
+                      reinterpret_cast<int*>(ws + L.lens),
+                      reinterpret_cast<int*>(ws + L.page_prefix),
+                      reinterpret_cast<int*>(ws + L.first_split),
+                      reinterpret_cast<int*>(ws + L.slot_base), reinterpret_cast<int*>(ws + L.meta),
+                      ctx->status};
     prof_mark(ctx, st, "absorb_q");
     ctx->launches += 1;
     if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
@@ -239,8 +267,8 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   // ---- value up-projection: o_i = W^UV_i o_lat_i
   {
     WgPlan p{};
-    p.nt = bp.nt;
-    p.n_tiles = bp.n_tiles;
+    p.nt = bp.uv.nt;
+    p.n_tiles = bp.uv.n_tiles;
     p.m_tiles = kHeads;
     p.tmA = ctx->tm_wuv;
     p.tmA2 = ctx->tm_wuv;
@@ -252,7 +280,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     a = base_args(ctx);
     a.n_tokens = M;
     a.k_chunks = kLat / 64;
-    a.splits = bp.s_uv;
+    a.splits = bp.uv.splits;
     a.tiles_per_head = 1;
     a.a_head_rows = kDv;
     a.b_head_cols = kLat;
@@ -267,8 +295,8 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   // ---- output projection: u = W_O o
   {
     WgPlan p{};
-    p.nt = bp.nt;
-    p.n_tiles = bp.n_tiles;
+    p.nt = bp.o.nt;
+    p.n_tiles = bp.o.n_tiles;
     p.m_tiles = D / 128;
     p.tmA = ctx->tm_wo;
     p.tmA2 = ctx->tm_wo;
@@ -280,7 +308,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     a = base_args(ctx);
     a.n_tokens = M;
     a.k_chunks = kHeads * kDv / 64;
-    a.splits = bp.s_o;
+    a.splits = bp.o.splits;
     a.tiles_per_head = D / 128;
     a.out = out;
     a.ld_out = D;

@@ -74,8 +74,9 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           const int32_t* pos, const int32_t* bt, int max_pages,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st);
 bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
-                 int num_pages, const int32_t* bt, int max_pages, int B, int T,
-                 __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
+                 int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
+                 int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
+                 cudaStream_t st);
 
 // bf16 path helpers
 bool bf16_setup(mla_ctx* ctx);                 // weight maps + scratch, at create

@@ -14,108 +14,25 @@
 //   * slot_base[b]   = partial-result slots of sequences 0..b-1; split c's
 //     piece of sequence b lands in slot slot_base[b] + c - first_split[b].
 // Every split does the same number of pages (+-1), whatever the length mix.
-#include "device_util.cuh"
+#include "plan_device.cuh"
 
 namespace mla {
 
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kMinPagesPerSplit = 2;
-
-__device__ __forceinline__ long long split_of_page(long long g, long long P, int G) {
-  return ((g + 1) * G - 1) / P;
-}
-
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ int block_exclusive_scan(int v, int* out, int* tmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int s = (lane < (int)(blockDim.x >> 5)) ? tmp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    tmp[lane] = s;  // inclusive warp totals
-  }
-  __syncthreads();
-  const int total = tmp[(blockDim.x >> 5) - 1];
-  *out = x - v + (warp > 0 ? tmp[warp - 1] : 0);
-  __syncthreads();
-  return total;
-}
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int page, int max_pages,
             int max_position, int G_max, int* lens, int* prefix, int* first_split,
             int* slot_base, int* meta, int* status) {
-  __shared__ int tmp[32];
-  __shared__ int carry;
+  __shared__ int tmp[33];
   // seq_lens may have been written by the kernel before us
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  // pass 1: validated lengths and the page prefix
-  for (int base = 0; base < B; base += kPlanThreads) {
-    const int b = base + threadIdx.x;
-    int pages = 0;
-    if (b < B) {
-      int len = seq_lens[b];
-      const int cap = min(max_pages * page, max_position);
-      if (len < T || len > cap) {
-        report(status, MLA_ERR_DEVICE_INDEX, 1000000 + b);
-        len = len < T ? T : cap;
-      }
-      lens[b] = len;
-      pages = (len + page - 1) / page;
-    }
-    int ex;
-    const int tot = block_exclusive_scan(pages, &ex, tmp);
-    if (b < B) prefix[b] = carry + ex;
-    __syncthreads();
-    if (threadIdx.x == 0) carry += tot;
-    __syncthreads();
-  }
-  const long long P = carry;
-  long long g_want = P / kMinPagesPerSplit;
-  if (g_want < 1) g_want = 1;
-  const int G = g_want < G_max ? (int)g_want : G_max;
-  if (threadIdx.x == 0) {
-    prefix[B] = carry;
-    meta[0] = G;
-    meta[1] = carry;
-  }
-  __syncthreads();
-  // pass 2: splits per sequence and their slot bases
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  for (int base = 0; base < B; base += kPlanThreads) {
-    const int b = base + threadIdx.x;
-    int ns = 0;
-    if (b < B) {
-      const long long c0 = split_of_page(prefix[b], P, G);
-      const long long c1 = split_of_page(prefix[b + 1] - 1, P, G);
-      first_split[b] = (int)c0;
-      ns = (int)(c1 - c0 + 1);
-    }
-    int ex;
-    const int tot = block_exclusive_scan(ns, &ex, tmp);
-    if (b < B) slot_base[b] = carry + ex;
-    __syncthreads();
-    if (threadIdx.x == 0) carry += tot;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) slot_base[B] = carry;
+  PlanArgs pa{seq_lens, B, T, page, max_pages, max_position, G_max, lens, prefix, first_split,
+              slot_base, meta, status};
+  build_plan<kPlanThreads>(threadIdx.x, [] { __syncthreads(); }, tmp, pa);
 }
 
 __global__ void selftest_wait_kernel(int spin_limit, int* status) {

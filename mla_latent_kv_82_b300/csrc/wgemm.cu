@@ -30,7 +30,7 @@ template <int NT> struct WgCfg {
   static constexpr uint32_t kB = NT * 64 * 2;
   static constexpr uint32_t kStage = kA + kB;
   static constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
-  static constexpr uint32_t kSmem = kStages * kStage + 1024 + 256;
+  static constexpr uint32_t kSmem = kStages * kStage + 1024 + 512;
 };
 
 constexpr int kThreads = 192;
@@ -55,6 +55,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   uint64_t* done = empty + S;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);   // abort, last, go
+  int* scan_tmp = reinterpret_cast<int*>(smem + S * C::kStage + 256);     // 33 ints
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, nt = blockIdx.y, z = blockIdx.z;
@@ -159,6 +160,8 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const int row = q * 32 + lane;
     const int etid = threadIdx.x - 64;   // 0..127
     const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    if (EPI == WG_QIMG && a.do_plan && mt == 0 && nt == 0 && z == 0)
+      build_plan<128>(etid, [] { tc::named_sync(2, 128); }, scan_tmp, a.plan);
     if (!mbar_wait(done, 0, a.status, 13)) flags[0] = 1;
     tc::fence_after_sync();
     // one decision for all 128 epilogue threads before any named barrier
@@ -237,17 +240,6 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             }
           }
         }
-        if constexpr (EPI == WG_QIMG) {
-          const int f = tile * 128 + row;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + j;
-            if (t < a.n_tokens)
-              *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.qimg) +
-                                           (size_t)t * kQImgBytes + qimg_off(head, f)) =
-                  bf16_bits(v[j]);
-          }
-        } else {
         // stage 16 tokens x 128 rows as bf16, then 16-byte stores per token row
 #pragma unroll
         for (int j = 0; j < 16; ++j) stg[j * kStgPitch + row] = bf16_bits(v[j]);
@@ -260,6 +252,11 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           __nv_bfloat16* dst = nullptr;
           if (EPI == WG_ROWMAJOR) {
             dst = a.out + (size_t)t * a.ld_out + head * a.out_head_cols + tile * 128 + ch * 8;
+          } else if (EPI == WG_QIMG) {
+            // 8 consecutive features of one head are one 16-byte chunk of the image
+            dst = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(a.qimg) +
+                                                   (size_t)t * kQImgBytes +
+                                                   qimg_off(head, tile * 128 + ch * 8));
           } else {   // WG_APPEND
             const int pos = a.pos[t];
             const int b = t / a.T;
@@ -278,23 +275,29 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
           *reinterpret_cast<uint4*>(dst) = val;
         }
         tc::named_sync(1, 128);
-        }
       }
       if (EPI == WG_QIMG && tile == 0) {
-        // rotated q^R of this head for the tile's tokens -> image features 512..575
-        for (int e = etid; e < NT * 32; e += 128) {
-          const int t = nt * NT + (e >> 5), j = e & 31;
+        // rotated q^R of this head for the tile's tokens -> image features
+        // 512..575, one 16-byte chunk (4 RoPE pairs) per step
+        for (int e = etid; e < NT * 8; e += 128) {
+          const int t = nt * NT + (e >> 3), ch = e & 7;
           if (t >= a.n_tokens) continue;
           const int b = t / a.T, tq = t % a.T;
-          const int pos = a.lens[b] - a.T + tq;
-          const __nv_bfloat16* qr = a.q + ((size_t)t * kHeads + head) * (kNope + kRope) + kNope;
-          const float x0 = __bfloat162float(qr[2 * j]), x1 = __bfloat162float(qr[2 * j + 1]);
-          const float2 cs = a.rope_cs[(size_t)pos * (kRope / 2) + j];
-          uint8_t* img = reinterpret_cast<uint8_t*>(a.qimg) + (size_t)t * kQImgBytes;
-          *reinterpret_cast<uint16_t*>(img + qimg_off(head, kLat + 2 * j)) =
-              bf16_bits(x0 * cs.x - x1 * cs.y);
-          *reinterpret_cast<uint16_t*>(img + qimg_off(head, kLat + 2 * j + 1)) =
-              bf16_bits(x0 * cs.y + x1 * cs.x);
+          const int pos = plan_len(a.plan.seq_lens, b, a.T, kPage, a.plan.max_pages,
+                                   a.max_position) - a.T + tq;
+          const uint4 raw = *reinterpret_cast<const uint4*>(
+              a.q + ((size_t)t * kHeads + head) * (kNope + kRope) + kNope + ch * 8);
+          const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
+          uint32_t o[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float x0 = __bfloat162float(x[2 * p]), x1 = __bfloat162float(x[2 * p + 1]);
+            const float2 cs = a.rope_cs[(size_t)pos * (kRope / 2) + ch * 4 + p];
+            o[p] = (uint32_t)bf16_bits(x0 * cs.x - x1 * cs.y) |
+                   ((uint32_t)bf16_bits(x0 * cs.y + x1 * cs.x) << 16);
+          }
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.qimg) + (size_t)t * kQImgBytes +
+                                    qimg_off(head, kLat + ch * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
     }

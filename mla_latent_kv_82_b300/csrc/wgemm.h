@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "plan_device.cuh"
+
 namespace mla {
 
 enum WgEpi { WG_ROWMAJOR = 0, WG_APPEND = 1, WG_QIMG = 2 };
@@ -28,10 +30,13 @@ struct WgArgs {
   const int32_t* bt;
   int max_pages, num_pages, T, max_position, append_rope_tile;
   const float2* rope_cs;
-  // WG_QIMG: absorbed-query image per token; RoPE of q^R by tile-0 CTAs
+  // WG_QIMG: absorbed-query image per token; RoPE of q^R by tile-0 CTAs at
+  // the position plan_len(seq_lens) - T + t; with do_plan, the epilogue
+  // warps of CTA 0 also build the split-KV plan while the MMAs run
   __nv_bfloat16* qimg;
   const __nv_bfloat16* q;
-  const int* lens;
+  PlanArgs plan;
+  int do_plan;
   // split-K scratch: partials [m_tiles * n_tiles * splits * NT * 128] fp32,
   // counters [m_tiles * n_tiles] (zero between launches)
   float* partials;
