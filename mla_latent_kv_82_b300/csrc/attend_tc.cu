@@ -104,6 +104,45 @@ __device__ __forceinline__ int nslabs_of(int tile_start, int p1) {
   return v >= kTile ? 4 : (v + 31) / 32;
 }
 
+// Pool row of token p of sequence sb (page id from the block table; a bad id
+// is reported and replaced by page 0 so that the TMA stays in bounds).
+__device__ __forceinline__ int page_row(const AttArgs& a, int sb, int p) {
+  int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
+  if (pg < 0 || pg >= a.num_pages) {
+    report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
+    pg = 0;
+  }
+  return pg * kPage;
+}
+
+// The pages of the tile starting at ts into L2 (each page is 64 x 1152
+// contiguous bytes), so that the ring's TMA loads of it hit L2.
+__device__ __forceinline__ void prefetch_tile(const AttArgs& a, int sb, int ts, int p1) {
+  for (int pp = 0; pp < 2 && ts + pp * kPage < p1; ++pp) {
+    const int pg = a.bt[(size_t)sb * a.max_pages + (ts + pp * kPage) / kPage];
+    if (pg >= 0 && pg < a.num_pages)
+      tc::prefetch_l2(a.cache + (size_t)pg * kPage * kRow, kPage * kRow * 2);
+  }
+}
+
+// Rows vis..31 of a value slab hold stale pool data past the visible end:
+// zero them so that 0 * (Inf or NaN) cannot reach the accumulator.  The slab
+// is 4 SW128 blocks of 32 rows x 128 B; the 32 lanes of a warp share the
+// 16-byte chunks, and each makes its writes visible to the tensor cores.
+__device__ __forceinline__ void zero_stale_rows(uint8_t* slab, int vis, int lane) {
+  for (int e = vis * 32 + lane; e < 32 * 32; e += 32) {
+    const int r = e >> 5, f = (e >> 3) & 3, ch = e & 7;
+    *reinterpret_cast<uint4*>(slab + f * 4096 + (r >> 3) * 1024 + (r & 7) * 128 + ch * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  tc::fence_async_smem();
+}
+
+// Bounded wait by a whole warp; the outcome is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int where) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
+}
+
 __global__ void __launch_bounds__(192, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
                  const AttArgs a) {
@@ -114,8 +153,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   uint64_t* full = bar;          // [kRing]
   uint64_t* empty = bar + 8;     // [kRing]
   uint64_t* s_full = bar + 16;   // [2] S buffer g&1 holds S(g)
-  uint64_t* p_full = bar + 18;   // P(g) written
-  uint64_t* pv_done = bar + 19;  // PV(g) done
+  // P(g) written: two barriers by tile parity, so the softmax warps, which
+  // may finish tile g+1 before the MMA thread waits for tile g, never move
+  // one barrier two phases past its waiter
+  uint64_t* const p_full = bar + 18;   // tile g: p_full + 6 * (g & 1)
+  // PV(g) done, also by tile parity: a waiter for PV(g) has always seen
+  // PV(g-2) complete (it precedes S(g) in the MMA pipe) and PV(g+2) cannot
+  // start before that waiter's own P(g+2)
+  uint64_t* const pv_done = bar + 19;  // tile g: pv_done + 6 * (g & 1)
   uint64_t* q_full = bar + 20;
   uint64_t* q_empty = bar + 21;
   uint64_t* o_free = bar + 22;
@@ -136,7 +181,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(p_full, 128);
+    mbar_init(p_full + 6, 128);
     mbar_init(pv_done, 1);
+    mbar_init(pv_done + 6, 1);
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(o_free, 128);
@@ -162,181 +209,162 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   int issued = 0;   // producer: ring stages issued
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      int rc = 0;
-      auto acquire = [&]() -> int {
-        const int s = rc % kRing;
-        if (rc >= kRing && !mbar_wait(&empty[s], ((rc / kRing) - 1) & 1, a.status, 22)) {
-          *abort_flag = 1;
-          return -1;
-        }
-        if (*abort_flag) return -1;
-        tc::mbar_arrive_expect_tx(smem_u32(&full[s]), kStage);
-        ++rc;
-        issued = rc;
-        return s;
-      };
-      auto page_row = [&](int sb, int p) -> int {
-        int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
-        if (pg < 0 || pg >= a.num_pages) {
-          report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
-          pg = 0;
-        }
-        return pg * kPage;
-      };
-      auto load_scores = [&](int sb, int ts, int p1) -> bool {
-        const int y0 = page_row(sb, ts);
-        const int y1 = ts + kPage < p1 ? page_row(sb, ts + kPage) : oob_row;
-        for (int b = 0; b < 9; ++b) {
-          const int s = acquire();
-          if (s < 0) return false;
-          const uint32_t dst = sR + s * kStage;
-          tc::tma_load_2d(dst, &tmS, b * 64, y0, smem_u32(&full[s]));
-          tc::tma_load_2d(dst + 8192, &tmS, b * 64, y1, smem_u32(&full[s]));
-        }
-        return true;
-      };
-      // pages of the tile starting at ts into L2, so the ring's TMA loads hit
-      // L2 instead of waiting on HBM (each page is 64 x 1152 contiguous bytes)
-      auto prefetch_tile = [&](int sb, int ts, int p1) {
-        for (int pp = 0; pp < 2 && ts + pp * kPage < p1; ++pp) {
-          const int pg = a.bt[(size_t)sb * a.max_pages + (ts + pp * kPage) / kPage];
-          if (pg >= 0 && pg < a.num_pages)
-            tc::prefetch_l2(a.cache + (size_t)pg * kPage * kRow, kPage * kRow * 2);
-        }
-      };
-      auto load_values = [&](int sb, int ts, int p1) -> bool {
-        const int ns = nslabs_of(ts, p1);
-        for (int v = 0; v < ns; ++v) {
-          const int s = acquire();
-          if (s < 0) return false;
-          const int p = ts + 32 * v;
-          const int y = page_row(sb, p) + (p % kPage);
-          const uint32_t dst = sR + s * kStage;
-          for (int f = 0; f < 4; ++f)
-            tc::tma_load_2d(dst + f * 4096, &tmV, half * 256 + f * 64, y, smem_u32(&full[s]));
-        }
-        return true;
-      };
-      SegIter it;
-      it.init(&a, c, t);
-      int sb, p0, p1, slot, k = 0;
-      bool ok = true;
-      while (ok && it.next(&sb, &p0, &p1, &slot)) {
-        const int n = ntiles_of(p0, p1);
-        if (n == 0) continue;
-        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status, 21)) { ok = false; break; }
-        if (*abort_flag) { ok = false; break; }
+    // -------------------------------------------------------------- producer
+    // The whole warp runs the loop with identical (warp-uniform) values and
+    // one elected lane issues the copies: a single divergent lane would keep
+    // every operand in per-thread registers and pay a conversion per issue.
+    // Per segment: the query image, then step i = 0..n loads the 9 score
+    // blocks of tile i (i < n) followed by the value slabs of tile i-1
+    // (i >= 1), the order in which the MMA warp consumes them.
+    const bool leader = tc::elect_one();
+    int rc = 0;   // ring stages issued
+    SegIter it;
+    it.init(&a, c, t);
+    int sb, p0, p1, slot, k = 0;
+    bool ok = true;
+    while (ok && it.next(&sb, &p0, &p1, &slot)) {
+      const int n = ntiles_of(p0, p1);
+      if (n == 0) continue;
+      if (k > 0 && !warp_wait(q_empty, (k - 1) & 1, a.status, 21)) { ok = false; break; }
+      if (*abort_flag) { ok = false; break; }
+      if (leader) {
         tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
         const uint8_t* qsrc = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes;
         for (int fb = 0; fb < 9; ++fb)
           tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
-        for (int i = 0; i < n && i < kPrefetchTiles; ++i) prefetch_tile(sb, p0 + i * kTile, p1);
-        ok = load_scores(sb, p0, p1);
-        for (int i = 0; ok && i < n; ++i) {
-          if (i + kPrefetchTiles < n) prefetch_tile(sb, p0 + (i + kPrefetchTiles) * kTile, p1);
-          if (i + 1 < n) ok = load_scores(sb, p0 + (i + 1) * kTile, p1);
-          if (ok) ok = load_values(sb, p0 + i * kTile, p1);
-        }
-        ++k;
+        for (int i = 0; i < n && i < kPrefetchTiles; ++i) prefetch_tile(a, sb, p0 + i * kTile, p1);
       }
-      if (!ok) *abort_flag = 1;
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idS = tc::idesc_bf16(128, kTile, false, false);
-      constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
-      // descriptors at offset 0; a K step adds (byte offset / 16)
-      const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
-      const uint64_t dR = tc::sdesc(sR, 16, 1024);
-      const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
-      int rc = 0, g = 0, k = 0, pv_issued = 0, pv_seen = 0;
-      bool ok = true;
-      // S(x) overwrites the buffer that held P(x-2): wait until every issued
-      // value MMA has finished.  At most one is ever outstanding, so each
-      // parity wait below targets the barrier's current or next phase.
-      auto drain_pv = [&]() -> bool {
-        while (pv_seen < pv_issued) {
-          if (!mbar_wait(pv_done, pv_seen & 1, a.status, 33)) return false;
-          ++pv_seen;
-        }
-        return true;
-      };
-      auto take = [&]() -> int {
-        const int s = rc % kRing;
-        if (!mbar_wait(&full[s], (rc / kRing) & 1, a.status, 23)) return -1;
-        tc::fence_after_sync();
-        ++rc;
-        return s;
-      };
-      auto issue_scores = [&](int gg) -> bool {
-        const uint32_t dcol = tmem + kColS + (gg & 1) * kTile;
-        for (int b = 0; b < 9; ++b) {
-          const int s = take();
-          if (s < 0) return false;
-          const uint64_t dRs = dR + ((s * kStage) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_ss(dcol, dQ + ((b * 16384 + kk * 32) >> 4), dRs + ((kk * 32) >> 4), idS,
-                       (b > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(smem_u32(&empty[s]));
-        }
-        tc::mma_commit(smem_u32(&s_full[gg & 1]));
-        return true;
-      };
-      SegIter it;
-      it.init(&a, c, t);
-      int sb, p0, p1, slot;
-      while (ok && it.next(&sb, &p0, &p1, &slot)) {
-        const int n = ntiles_of(p0, p1);
-        if (n == 0) continue;
-        if (!mbar_wait(q_full, k & 1, a.status, 24)) { ok = false; break; }
-        if (!(ok = drain_pv()) || !(ok = issue_scores(g))) break;
-        for (int i = 0; i < n; ++i, ++g) {
-          if (i + 1 < n && (!(ok = drain_pv()) || !(ok = issue_scores(g + 1)))) break;
-          if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
-          if (i == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, a.status, 25))) break;
-          if (!(ok = mbar_wait(p_full, g & 1, a.status, 26))) break;
-          if (*abort_flag) { ok = false; break; }
-          tc::fence_after_sync();
-          // at most one value MMA in flight, so pv_done is never two phases ahead
-          if (!(ok = drain_pv())) break;
+      __syncwarp();
+      for (int i = 0; ok && i <= n; ++i) {
+        if (leader && i + kPrefetchTiles < n)
+          prefetch_tile(a, sb, p0 + (i + kPrefetchTiles) * kTile, p1);
+        const int nsc = i < n ? 9 : 0;
+        const int tv = p0 + (i - 1) * kTile;   // tile whose value slabs follow
+        const int nv = i >= 1 ? nslabs_of(tv, p1) : 0;
+        int y0 = 0, y1 = 0;
+        if (nsc) {
           const int ts = p0 + i * kTile;
-          const int ns = nslabs_of(ts, p1);
-          for (int v = 0; v < ns; ++v) {
-            const int s = take();
-            if (s < 0) { ok = false; break; }
-            const int vis = p1 - (ts + 32 * v);
-            if (vis < 32) {
-              // rows past the visible end hold stale pool data: zero them so
-              // that 0 * (Inf or NaN) cannot reach the accumulator
-              uint8_t* st0 = smem + kOffRing + s * kStage;
-              for (int e = vis * 32; e < 32 * 32; ++e) {
-                const int r = e >> 5, f = (e >> 3) & 3, ch = e & 7;
-                *reinterpret_cast<uint4*>(st0 + f * 4096 + (r >> 3) * 1024 + (r & 7) * 128 +
-                                          ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-              }
-              tc::fence_async_smem();
-            }
+          y0 = page_row(a, sb, ts);
+          y1 = ts + kPage < p1 ? page_row(a, sb, ts + kPage) : oob_row;
+        }
+        for (int j = 0; j < nsc + nv; ++j, ++rc) {
+          const int s = rc % kRing;
+          if (rc >= kRing && !warp_wait(&empty[s], ((rc / kRing) - 1) & 1, a.status, 22)) {
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[s]);
+          const uint32_t dst = sR + s * kStage;
+          int y = 0;
+          if (j >= nsc) {
+            const int pv = tv + 32 * (j - nsc);
+            y = page_row(a, sb, pv) + (pv % kPage);
+          }
+          issued = rc + 1;
+          if (leader) {
+            tc::mbar_arrive_expect_tx(fb, kStage);
+            if (j < nsc) {
+              tc::tma_load_2d(dst, &tmS, j * 64, y0, fb);
+              tc::tma_load_2d(dst + 8192, &tmS, j * 64, y1, fb);
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              // P tokens 32v+16kk.. live in columns (32v+16kk)/2.. of S buffer g&1
-              tc::mma_ts(tmem, tmem + kColS + (g & 1) * kTile + 16 * v + 8 * kk,
-                         dV + ((s * kStage + kk * 2048) >> 4), idO,
-                         (i > 0 || v > 0 || kk > 0) ? 1u : 0u);
+              for (int f = 0; f < 4; ++f)
+                tc::tma_load_2d(dst + f * 4096, &tmV, half * 256 + f * 64, y, fb);
             }
-            tc::mma_commit(smem_u32(&empty[s]));
+          }
+          __syncwarp();
+        }
+      }
+      ++k;
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    // Warp-uniform loop, one elected lane issues (as for the producer).  Same
+    // step order as the producer: S of tile i, then PV of tile i-1 once the
+    // softmax warps have written P(i-1).  S(x) overwrites the TMEM columns
+    // that held P(x-2); both come from the same issuing thread and the MMA
+    // pipe executes in issue order, so PV(x-2) has read P first.
+    const bool leader = tc::elect_one();
+    constexpr uint32_t idS = tc::idesc_bf16(128, kTile, false, false);
+    constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
+    // descriptors at offset 0; a K step adds (byte offset / 16)
+    const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
+    const uint64_t dR = tc::sdesc(sR, 16, 1024);
+    const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
+    int rc = 0, g = 0, k = 0;
+    bool ok = true;
+    SegIter it;
+    it.init(&a, c, t);
+    int sb, p0, p1, slot;
+    while (ok && it.next(&sb, &p0, &p1, &slot)) {
+      const int n = ntiles_of(p0, p1);
+      if (n == 0) continue;
+      if (!warp_wait(q_full, k & 1, a.status, 24)) { ok = false; break; }
+      for (int i = 0; ok && i <= n; ++i) {
+        if (i < n) {
+          const int gs = g + i;
+          const uint32_t dcol = tmem + kColS + (gs & 1) * kTile;
+          for (int b = 0; b < 9; ++b, ++rc) {
+            const int s = rc % kRing;
+            if (!warp_wait(&full[s], (rc / kRing) & 1, a.status, 23)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint64_t dRs = dR + ((s * kStage) >> 4);
+            const uint64_t dQb = dQ + ((b * 16384) >> 4);
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_ss(dcol, dQb + kk * 2, dRs + kk * 2, idS, (b > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_commit(smem_u32(&empty[s]));
+            }
+            __syncwarp();
           }
           if (!ok) break;
-          tc::mma_commit(smem_u32(pv_done));
-          ++pv_issued;
+          if (leader) {
+            tc::mma_commit(smem_u32(&s_full[gs & 1]));
+            if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
+          }
+          __syncwarp();
         }
-        ++k;
+        if (i >= 1) {
+          const int gv = g + i - 1;
+          const int tv = p0 + (i - 1) * kTile;
+          if (i == 1 && k > 0 && !warp_wait(o_free, (k - 1) & 1, a.status, 25)) { ok = false; break; }
+          if (!warp_wait(p_full + 6 * (gv & 1), (gv >> 1) & 1, a.status, 26)) { ok = false; break; }
+          if (*abort_flag) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
+          const int ns = nslabs_of(tv, p1);
+          for (int v = 0; v < ns; ++v, ++rc) {
+            const int s = rc % kRing;
+            if (!warp_wait(&full[s], (rc / kRing) & 1, a.status, 23)) { ok = false; break; }
+            tc::fence_after_sync();
+            const int vis = p1 - (tv + 32 * v);
+            if (vis < 32) {
+              zero_stale_rows(smem + kOffRing + s * kStage, vis, lane);
+              __syncwarp();
+            }
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                // P tokens 32v+16kk.. live in columns (32v+16kk)/2.. of the S buffer
+                tc::mma_ts(tmem, pcol + 16 * v + 8 * kk, dV + ((s * kStage + kk * 2048) >> 4),
+                           idO, (i > 1 || v > 0 || kk > 0) ? 1u : 0u);
+              }
+              tc::mma_commit(smem_u32(&empty[s]));
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (leader) tc::mma_commit(smem_u32(pv_done + 6 * (gv & 1)));
+          __syncwarp();
+        }
       }
-      if (!ok) *abort_flag = 1;
+      g += n;
+      ++k;
     }
+    if (!ok) *abort_flag = 1;
   } else {
     // ------------------------------------------------------------ softmax warps
     const int q4 = warp & 3;
@@ -373,16 +401,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             if (c0 + j < valid) mx = fmaxf(mx, x[j]);
         }
         mx *= a.scale_log2;
-        if (i > 0) {
-          // P buffer reuse and a possible O rescale both need PV(g-1) done
-          ok = mbar_wait(pv_done, (g - 1) & 1, a.status, 28);
-          if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-          tc::fence_after_sync();
-        }
+        // S(g) done implies every earlier value MMA but PV(g-1) is done, so
+        // P(g) may overwrite S(g) now; only a rescale of O waits for PV(g-1).
         const bool need = mx > m_used + kRescale;
         if (i == 0) {
           m_used = mx;
         } else if (__any_sync(0xffffffffu, need)) {
+          ok = mbar_wait(pv_done + 6 * ((g - 1) & 1), ((g - 1) >> 1) & 1, a.status, 28);
+          if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+          tc::fence_after_sync();
           const float m_new = need ? mx : m_used;
           const float f = exp2f(m_used - m_new);
           l *= f;
@@ -423,11 +450,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         }
         l += psum;
         tc::fence_before_sync();
-        tc::mbar_arrive(smem_u32(p_full));
+        tc::mbar_arrive(smem_u32(p_full + 6 * (g & 1)));
       }
       if (!ok) break;
       // segment epilogue: O / l and the log-sum-exp
-      ok = mbar_wait(pv_done, (g - 1) & 1, a.status, 29);
+      // PV of the last tile done implies every earlier one is
+      ok = mbar_wait(pv_done + 6 * ((g - 1) & 1), ((g - 1) >> 1) & 1, a.status, 29);
       if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
       tc::fence_after_sync();
       const float inv = 1.f / l;

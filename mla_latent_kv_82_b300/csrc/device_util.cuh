@@ -46,13 +46,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the same condition.  When the phase has already
+// completed this returns in a fraction of the time try_wait takes, which
+// matters on the tensor-core issue path (one check per ring stage).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, polling at most `max_polls`
 // times and for at most `max_ns` nanoseconds.  On giving up, records
 // MLA_ERR_TIMEOUT with `where` as detail and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int where,
                                           long long max_polls = (1LL << 40),
                                           uint64_t max_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (long long i = 1; i < max_polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
