@@ -138,10 +138,62 @@ __device__ __forceinline__ void zero_stale_rows(uint8_t* slab, int vis, int lane
   tc::fence_async_smem();
 }
 
-// Bounded wait by a whole warp; the outcome is made warp-uniform.
+// Row maximum of the raw scores of tokens 0..valid-1 (lo: 0..63, hi: 64..127).
+template <bool kMask>
+__device__ __forceinline__ float row_max(const uint32_t (&lo)[64], const uint32_t (&hi)[64],
+                                         int valid) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    if (!kMask || j < valid) m0 = fmaxf(m0, __uint_as_float(lo[j]));
+    if (!kMask || 64 + j < valid) m1 = fmaxf(m1, __uint_as_float(hi[j]));
+  }
+  return fmaxf(m0, m1);
+}
+
+// p = 2^(s * scale_log2 - m) for tokens below `valid` (0 beyond), rounded to
+// bf16 and packed two per word: pk[j] holds tokens 2j (low) and 2j+1 (high).
+// Returns the sum of the fp32 values.
+template <bool kMask>
+__device__ __forceinline__ float exp_pack(const uint32_t (&lo)[64], const uint32_t (&hi)[64],
+                                          int valid, float scale_log2, float m,
+                                          uint32_t (&pk)[64]) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) {
+    const int t0 = 2 * j, t1 = 2 * j + 1;
+    const float x0 = __uint_as_float(t0 < 64 ? lo[t0] : hi[t0 - 64]);
+    const float x1 = __uint_as_float(t1 < 64 ? lo[t1] : hi[t1 - 64]);
+    const float e0 = (!kMask || t0 < valid) ? tc::ex2_approx(fmaf(x0, scale_log2, -m)) : 0.f;
+    const float e1 = (!kMask || t1 < valid) ? tc::ex2_approx(fmaf(x1, scale_log2, -m)) : 0.f;
+    s0 += e0;
+    s1 += e1;
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+    pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  return s0 + s1;
+}
+
+// Bounded wait by a whole warp; the outcome is made warp-uniform.  The
+// common case (phase already complete) costs one probe and one vote.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int where) {
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
 }
+
+// Position in the stage ring: slot, phase bit of this pass over the ring, and
+// the number of stages passed so far.
+struct RingPos {
+  int s = 0, n = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    ++n;
+    if (++s == kRing) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 
 __global__ void __launch_bounds__(192, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
@@ -217,7 +269,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     // blocks of tile i (i < n) followed by the value slabs of tile i-1
     // (i >= 1), the order in which the MMA warp consumes them.
     const bool leader = tc::elect_one();
-    int rc = 0;   // ring stages issued
+    RingPos rp;   // next stage to fill
     SegIter it;
     it.init(&a, c, t);
     int sb, p0, p1, slot, k = 0;
@@ -234,7 +286,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
         for (int i = 0; i < n && i < kPrefetchTiles; ++i) prefetch_tile(a, sb, p0 + i * kTile, p1);
       }
-      __syncwarp();
       for (int i = 0; ok && i <= n; ++i) {
         if (leader && i + kPrefetchTiles < n)
           prefetch_tile(a, sb, p0 + (i + kPrefetchTiles) * kTile, p1);
@@ -247,9 +298,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           y0 = page_row(a, sb, ts);
           y1 = ts + kPage < p1 ? page_row(a, sb, ts + kPage) : oob_row;
         }
-        for (int j = 0; j < nsc + nv; ++j, ++rc) {
-          const int s = rc % kRing;
-          if (rc >= kRing && !warp_wait(&empty[s], ((rc / kRing) - 1) & 1, a.status, 22)) {
+        for (int j = 0; j < nsc + nv; ++j, rp.next()) {
+          const int s = rp.s;
+          // the stage's previous pass must have been consumed
+          if (rp.n >= kRing && !warp_wait(&empty[s], rp.ph ^ 1u, a.status, 22)) {
             ok = false;
             break;
           }
@@ -261,7 +313,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             const int pv = tv + 32 * (j - nsc);
             y = page_row(a, sb, pv) + (pv % kPage);
           }
-          issued = rc + 1;
+          issued = rp.n + 1;
           if (leader) {
             tc::mbar_arrive_expect_tx(fb, kStage);
             if (j < nsc) {
@@ -273,7 +325,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 tc::tma_load_2d(dst + f * 4096, &tmV, half * 256 + f * 64, y, fb);
             }
           }
-          __syncwarp();
         }
       }
       ++k;
@@ -293,7 +344,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
     const uint64_t dR = tc::sdesc(sR, 16, 1024);
     const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
-    int rc = 0, g = 0, k = 0;
+    RingPos rp;   // next stage to consume
+    int g = 0, k = 0;
     bool ok = true;
     SegIter it;
     it.init(&a, c, t);
@@ -306,9 +358,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (i < n) {
           const int gs = g + i;
           const uint32_t dcol = tmem + kColS + (gs & 1) * kTile;
-          for (int b = 0; b < 9; ++b, ++rc) {
-            const int s = rc % kRing;
-            if (!warp_wait(&full[s], (rc / kRing) & 1, a.status, 23)) { ok = false; break; }
+          for (int b = 0; b < 9; ++b, rp.next()) {
+            const int s = rp.s;
+            if (!warp_wait(&full[s], rp.ph, a.status, 23)) { ok = false; break; }
             tc::fence_after_sync();
             const uint64_t dRs = dR + ((s * kStage) >> 4);
             const uint64_t dQb = dQ + ((b * 16384) >> 4);
@@ -318,14 +370,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
                 tc::mma_ss(dcol, dQb + kk * 2, dRs + kk * 2, idS, (b > 0 || kk > 0) ? 1u : 0u);
               tc::mma_commit(smem_u32(&empty[s]));
             }
-            __syncwarp();
           }
           if (!ok) break;
           if (leader) {
             tc::mma_commit(smem_u32(&s_full[gs & 1]));
             if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
           }
-          __syncwarp();
         }
         if (i >= 1) {
           const int gv = g + i - 1;
@@ -336,9 +386,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           tc::fence_after_sync();
           const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
           const int ns = nslabs_of(tv, p1);
-          for (int v = 0; v < ns; ++v, ++rc) {
-            const int s = rc % kRing;
-            if (!warp_wait(&full[s], (rc / kRing) & 1, a.status, 23)) { ok = false; break; }
+          for (int v = 0; v < ns; ++v, rp.next()) {
+            const int s = rp.s;
+            if (!warp_wait(&full[s], rp.ph, a.status, 23)) { ok = false; break; }
             tc::fence_after_sync();
             const int vis = p1 - (tv + 32 * v);
             if (vis < 32) {
@@ -354,11 +404,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
               }
               tc::mma_commit(smem_u32(&empty[s]));
             }
-            __syncwarp();
           }
           if (!ok) break;
           if (leader) tc::mma_commit(smem_u32(pv_done + 6 * (gv & 1)));
-          __syncwarp();
         }
       }
       g += n;
@@ -391,15 +439,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
         const int valid = min(kTile, p1 - (p0 + i * kTile));
-        // pass 1: row maximum over the visible tokens of the tile
-        float mx = -INFINITY;
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
-          float x[16];
-          tc::tmem_ld16(scol + c0, x);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < valid) mx = fmaxf(mx, x[j]);
-        }
+        // the whole S row of this tile (128 tokens) into registers
+        uint32_t lo[64], hi[64];
+        tc::tmem_ld64(scol, lo);
+        tc::tmem_ld64(scol + 64, hi);
+        float mx = valid == kTile ? row_max<false>(lo, hi, valid) : row_max<true>(lo, hi, valid);
         mx *= a.scale_log2;
         // S(g) done implies every earlier value MMA but PV(g-1) is done, so
         // P(g) may overwrite S(g) now; only a rescale of O waits for PV(g-1).
@@ -422,32 +466,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           }
           m_used = m_new;
         }
-        // pass 2: P = 2^(s*scale - m) as bf16, written over the S columns
-        // already read (tokens c0..c0+31 -> columns c0/2..c0/2+15)
-        float psum = 0.f;
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
-          float x[32];
-          {
-            float v[16];
-            tc::tmem_ld16(scol + c0, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) x[j] = v[j];
-            tc::tmem_ld16(scol + c0 + 16, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) x[16 + j] = v[j];
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float e0 = c0 + 2 * j < valid ? exp2f(fmaf(x[2 * j], a.scale_log2, -m_used)) : 0.f;
-            const float e1 =
-                c0 + 2 * j + 1 < valid ? exp2f(fmaf(x[2 * j + 1], a.scale_log2, -m_used)) : 0.f;
-            psum += e0 + e1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-            pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          tc::tmem_st16_u32(scol + (c0 >> 1), pk);
-        }
+        // P = 2^(s*scale - m) as bf16, packed two per column over the S
+        // columns (tokens 2j, 2j+1 -> column j)
+        uint32_t pk[64];
+        const float psum = valid == kTile
+                               ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
+                               : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
+        tc::tmem_st64(scol, pk);
         l += psum;
         tc::fence_before_sync();
         tc::mbar_arrive(smem_u32(p_full + 6 * (g & 1)));
