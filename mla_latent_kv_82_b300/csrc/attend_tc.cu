@@ -20,13 +20,15 @@
 // as score blocks [128 tokens x 64 features] (one per feature block), then
 // as value slabs [32 tokens x 256 features of this half].
 //
-// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM
-// owner, warps 2-5 = softmax (thread = head): online softmax in the log2
-// domain with a lazy rescale (O and l are rescaled only when a row maximum
-// grows by more than 2^8, so P <= 256), P packed two bf16 per TMEM column.  At the end of a segment the same warps
-// write O / l and m + log2 l for the log-sum-exp combine.  Every wait is
-// bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains its own
-// loads and frees TMEM.
+// Roles (224 threads): warp 0 = TMA producer, warp 1 = score-MMA issuer and
+// TMEM owner, warp 6 = value-MMA issuer (two issuing threads, so that the
+// per-stage issue overhead of the two streams overlaps), warps 2-5 = softmax
+// (thread = head): online softmax in the log2 domain with a lazy rescale (O
+// and l are rescaled only when a row maximum grows by more than 2^8, so
+// P <= 256), P packed two bf16 per TMEM column.  At the end of a segment the
+// same warps write O / l and m + log2 l for the log-sum-exp combine.  Every
+// wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains its
+// own loads and frees TMEM.
 #include "layouts.cuh"
 #include "tc_util.cuh"
 #include "mla_internal.h"
@@ -45,7 +47,6 @@ constexpr uint32_t kSmem = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;                            // S buffers at 256 and 384
 constexpr float kRescale = 8.0f;                           // log2 units
-constexpr int kPrefetchTiles = 3;                          // L2 prefetch distance
 
 struct AttArgs {
   const int* lens;
@@ -113,16 +114,6 @@ __device__ __forceinline__ int page_row(const AttArgs& a, int sb, int p) {
     pg = 0;
   }
   return pg * kPage;
-}
-
-// The pages of the tile starting at ts into L2 (each page is 64 x 1152
-// contiguous bytes), so that the ring's TMA loads of it hit L2.
-__device__ __forceinline__ void prefetch_tile(const AttArgs& a, int sb, int ts, int p1) {
-  for (int pp = 0; pp < 2 && ts + pp * kPage < p1; ++pp) {
-    const int pg = a.bt[(size_t)sb * a.max_pages + (ts + pp * kPage) / kPage];
-    if (pg >= 0 && pg < a.num_pages)
-      tc::prefetch_l2(a.cache + (size_t)pg * kPage * kRow, kPage * kRow * 2);
-  }
 }
 
 // Rows vis..31 of a value slab hold stale pool data past the visible end:
@@ -193,9 +184,12 @@ struct RingPos {
       ph ^= 1u;
     }
   }
+  __device__ __forceinline__ void skip(int m) {
+    for (int j = 0; j < m; ++j) next();
+  }
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
                  const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -213,6 +207,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   // PV(g-2) complete (it precedes S(g) in the MMA pipe) and PV(g+2) cannot
   // start before that waiter's own P(g+2)
   uint64_t* const pv_done = bar + 19;  // tile g: pv_done + 6 * (g & 1)
+  uint64_t* const drained = bar + 26;   // both MMA issuers' last MMAs done
   uint64_t* q_full = bar + 20;
   uint64_t* q_empty = bar + 21;
   uint64_t* o_free = bar + 22;
@@ -239,6 +234,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(o_free, 128);
+    mbar_init(drained, 2);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -258,7 +254,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sR = smem_u32(smem + kOffRing);
   const int oob_row = a.num_pages * kPage + kPage;   // TMA zero-fills rows out of range
-  int issued = 0;   // producer: ring stages issued
+  int issued = 0;     // producer: ring stages issued
+  int q_issued = 0;   // producer: query images issued
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
@@ -279,16 +276,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       if (n == 0) continue;
       if (k > 0 && !warp_wait(q_empty, (k - 1) & 1, a.status, 21)) { ok = false; break; }
       if (*abort_flag) { ok = false; break; }
+      ++q_issued;
       if (leader) {
         tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
         const uint8_t* qsrc = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes;
         for (int fb = 0; fb < 9; ++fb)
           tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
-        for (int i = 0; i < n && i < kPrefetchTiles; ++i) prefetch_tile(a, sb, p0 + i * kTile, p1);
       }
       for (int i = 0; ok && i <= n; ++i) {
-        if (leader && i + kPrefetchTiles < n)
-          prefetch_tile(a, sb, p0 + (i + kPrefetchTiles) * kTile, p1);
         const int nsc = i < n ? 9 : 0;
         const int tv = p0 + (i - 1) * kTile;   // tile whose value slabs follow
         const int nv = i >= 1 ? nslabs_of(tv, p1) : 0;
@@ -331,20 +326,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     }
     if (!ok) *abort_flag = 1;
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    // Warp-uniform loop, one elected lane issues (as for the producer).  Same
-    // step order as the producer: S of tile i, then PV of tile i-1 once the
-    // softmax warps have written P(i-1).  S(x) overwrites the TMEM columns
-    // that held P(x-2); both come from the same issuing thread and the MMA
-    // pipe executes in issue order, so PV(x-2) has read P first.
+    // -------------------------------------------------------- score-MMA issuer
+    // Warp-uniform loop, one elected lane issues (as for the producer).  It
+    // consumes the score stages of the ring and steps over the value stages,
+    // which the value-MMA warp consumes.  S(x) overwrites the TMEM columns
+    // that held P(x-2), so it first waits for PV(x-2) to complete.
     const bool leader = tc::elect_one();
     constexpr uint32_t idS = tc::idesc_bf16(128, kTile, false, false);
-    constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
     // descriptors at offset 0; a K step adds (byte offset / 16)
     const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
     const uint64_t dR = tc::sdesc(sR, 16, 1024);
-    const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
-    RingPos rp;   // next stage to consume
+    RingPos rp;   // next stage in ring order
     int g = 0, k = 0;
     bool ok = true;
     SegIter it;
@@ -357,6 +349,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       for (int i = 0; ok && i <= n; ++i) {
         if (i < n) {
           const int gs = g + i;
+          if (gs >= 2 &&
+              !warp_wait(pv_done + 6 * (gs & 1), ((gs - 2) >> 1) & 1, a.status, 33)) {
+            ok = false;
+            break;
+          }
           const uint32_t dcol = tmem + kColS + (gs & 1) * kTile;
           for (int b = 0; b < 9; ++b, rp.next()) {
             const int s = rp.s;
@@ -377,11 +374,45 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             if (i == n - 1) tc::mma_commit(smem_u32(q_empty));
           }
         }
+        if (i >= 1) rp.skip(nslabs_of(p0 + (i - 1) * kTile, p1));   // value stages of tile i-1
+      }
+      g += n;
+      ++k;
+    }
+    if (!ok) *abort_flag = 1;
+    if (leader) tc::mma_commit(smem_u32(drained));
+  } else if (warp == 6) {
+    // -------------------------------------------------------- value-MMA issuer
+    // Steps over the score stages; for tile x waits for P(x) from the
+    // softmax warps, then O += P(x) V(x) from the value slabs.
+    const bool leader = tc::elect_one();
+    constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
+    const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
+    RingPos rp;
+    int g = 0, k = 0;
+    bool ok = true;
+    SegIter it;
+    it.init(&a, c, t);
+    int sb, p0, p1, slot;
+    while (ok && it.next(&sb, &p0, &p1, &slot)) {
+      const int n = ntiles_of(p0, p1);
+      if (n == 0) continue;
+      for (int i = 0; ok && i <= n; ++i) {
+        if (i < n) rp.skip(9);   // score stages of tile i
         if (i >= 1) {
           const int gv = g + i - 1;
           const int tv = p0 + (i - 1) * kTile;
           if (i == 1 && k > 0 && !warp_wait(o_free, (k - 1) & 1, a.status, 25)) { ok = false; break; }
           if (!warp_wait(p_full + 6 * (gv & 1), (gv >> 1) & 1, a.status, 26)) { ok = false; break; }
+          // The value stages of tile x sit behind the score stages of tile
+          // x+1 in the ring.  This warp steps over those without waiting, so
+          // before waiting on its own slots it makes sure S(x+1) is done (all
+          // its stages filled): otherwise a slot's barrier could still be a
+          // whole lap behind, which a parity wait cannot tell apart.
+          if (i < n && !warp_wait(&s_full[(gv + 1) & 1], ((gv + 1) >> 1) & 1, a.status, 34)) {
+            ok = false;
+            break;
+          }
           if (*abort_flag) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
@@ -413,7 +444,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       ++k;
     }
     if (!ok) *abort_flag = 1;
-  } else {
+    if (leader) tc::mma_commit(smem_u32(drained));
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ softmax warps
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;          // head
@@ -507,10 +539,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       const int u = issued - 1 - i;
       mbar_wait(&full[u % kRing], (u / kRing) & 1, a.status, 30, 1 << 20, 100000000ull);
     }
-    mbar_wait(q_full, 0, a.status, 31, 1 << 20, 100000000ull);
+    if (q_issued > 0) mbar_wait(q_full, (q_issued - 1) & 1, a.status, 31, 1 << 20, 100000000ull);
   }
   __syncthreads();
   if (warp == 1) {
+    // TMEM is freed only once both issuing threads' MMAs have completed
+    mbar_wait(drained, 0, a.status, 32, 1 << 20, 100000000ull);
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -551,7 +585,7 @@ bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.G, T, 2);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(224);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
