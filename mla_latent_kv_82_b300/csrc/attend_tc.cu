@@ -29,165 +29,21 @@
 // same warps write O / l and m + log2 l for the log-sum-exp combine.  Every
 // wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT, drains its
 // own loads and frees TMEM.
-#include "layouts.cuh"
-#include "tc_util.cuh"
-#include "mla_internal.h"
+#include "attend_common.cuh"
 #include "tmap.h"
 
 namespace mla {
 namespace {
 
-constexpr int kTile = 128;                                 // tokens per tile (2 pages)
 constexpr int kRing = 5;                                   // ring stages
 constexpr uint32_t kStage = 16384;                         // one ring stage
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = kQImgBytes;                  // 147456
 constexpr uint32_t kOffBar = kOffRing + kRing * kStage;    // 229376
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256;                            // S buffers at 256 and 384
-constexpr float kRescale = 8.0f;                           // log2 units
 
-struct AttArgs {
-  const int* lens;
-  const int* prefix;
-  const int* first_split;
-  const int* slot_base;
-  const int* meta;
-  const int32_t* bt;
-  const uint8_t* qimg;
-  const __nv_bfloat16* cache;
-  float* part_o;
-  float* part_lse;
-  int* status;
-  int B, T, max_pages, num_pages;
-  float scale_log2;
-};
-
-// Iterates the (sequence, page range) segments of split c, in order.
-struct SegIter {
-  const AttArgs* a;
-  int c, t;
-  long long g0, g1;
-  int b;
-  __device__ void init(const AttArgs* args, int c_, int t_) {
-    a = args;
-    c = c_;
-    t = t_;
-    const int G = a->meta[0];
-    if (c >= G) { g0 = g1 = 0; b = a->B; return; }
-    split_range(c, a->prefix[a->B], G, &g0, &g1);
-    b = seq_of_page(a->prefix, a->B, g0);
-  }
-  // Next segment: sequence, first token, end token (exclusive, visible), slot.
-  __device__ bool next(int* sb, int* p0, int* p1, int* slot) {
-    if (b >= a->B || a->prefix[b] >= g1) return false;
-    const long long pb = a->prefix[b];
-    const long long lo = g0 > pb ? g0 : pb;
-    const long long hi = g1 < a->prefix[b + 1] ? g1 : a->prefix[b + 1];
-    const int vis = a->lens[b] - a->T + t + 1;
-    *sb = b;
-    *p0 = (int)(lo - pb) * kPage;
-    *p1 = min((int)(hi - pb) * kPage, vis);
-    *slot = a->slot_base[b] + (c - a->first_split[b]);
-    ++b;
-    return true;
-  }
-};
-
-__device__ __forceinline__ int ntiles_of(int p0, int p1) {
-  return p1 > p0 ? (p1 - p0 + kTile - 1) / kTile : 0;
-}
-
-// value slabs (32 tokens) of tile i that hold at least one visible token
-__device__ __forceinline__ int nslabs_of(int tile_start, int p1) {
-  const int v = p1 - tile_start;
-  return v >= kTile ? 4 : (v + 31) / 32;
-}
-
-// Pool row of token p of sequence sb (page id from the block table; a bad id
-// is reported and replaced by page 0 so that the TMA stays in bounds).
-__device__ __forceinline__ int page_row(const AttArgs& a, int sb, int p) {
-  int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
-  if (pg < 0 || pg >= a.num_pages) {
-    report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
-    pg = 0;
-  }
-  return pg * kPage;
-}
-
-// Rows vis..31 of a value slab hold stale pool data past the visible end:
-// zero them so that 0 * (Inf or NaN) cannot reach the accumulator.  The slab
-// is 4 SW128 blocks of 32 rows x 128 B; the 32 lanes of a warp share the
-// 16-byte chunks, and each makes its writes visible to the tensor cores.
-__device__ __forceinline__ void zero_stale_rows(uint8_t* slab, int vis, int lane) {
-  for (int e = vis * 32 + lane; e < 32 * 32; e += 32) {
-    const int r = e >> 5, f = (e >> 3) & 3, ch = e & 7;
-    *reinterpret_cast<uint4*>(slab + f * 4096 + (r >> 3) * 1024 + (r & 7) * 128 + ch * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-  tc::fence_async_smem();
-}
-
-// Row maximum of the raw scores of tokens 0..valid-1 (lo: 0..63, hi: 64..127).
-template <bool kMask>
-__device__ __forceinline__ float row_max(const uint32_t (&lo)[64], const uint32_t (&hi)[64],
-                                         int valid) {
-  float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    if (!kMask || j < valid) m0 = fmaxf(m0, __uint_as_float(lo[j]));
-    if (!kMask || 64 + j < valid) m1 = fmaxf(m1, __uint_as_float(hi[j]));
-  }
-  return fmaxf(m0, m1);
-}
-
-// p = 2^(s * scale_log2 - m) for tokens below `valid` (0 beyond), rounded to
-// bf16 and packed two per word: pk[j] holds tokens 2j (low) and 2j+1 (high).
-// Returns the sum of the fp32 values.
-template <bool kMask>
-__device__ __forceinline__ float exp_pack(const uint32_t (&lo)[64], const uint32_t (&hi)[64],
-                                          int valid, float scale_log2, float m,
-                                          uint32_t (&pk)[64]) {
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-  for (int j = 0; j < 64; ++j) {
-    const int t0 = 2 * j, t1 = 2 * j + 1;
-    const float x0 = __uint_as_float(t0 < 64 ? lo[t0] : hi[t0 - 64]);
-    const float x1 = __uint_as_float(t1 < 64 ? lo[t1] : hi[t1 - 64]);
-    const float e0 = (!kMask || t0 < valid) ? tc::ex2_approx(fmaf(x0, scale_log2, -m)) : 0.f;
-    const float e1 = (!kMask || t1 < valid) ? tc::ex2_approx(fmaf(x1, scale_log2, -m)) : 0.f;
-    s0 += e0;
-    s1 += e1;
-    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-    pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
-  }
-  return s0 + s1;
-}
-
-// Bounded wait by a whole warp; the outcome is made warp-uniform.  The
-// common case (phase already complete) costs one probe and one vote.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status, int where) {
-  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
-}
-
-// Position in the stage ring: slot, phase bit of this pass over the ring, and
-// the number of stages passed so far.
-struct RingPos {
-  int s = 0, n = 0;
-  uint32_t ph = 0;
-  __device__ __forceinline__ void next() {
-    ++n;
-    if (++s == kRing) {
-      s = 0;
-      ph ^= 1u;
-    }
-  }
-  __device__ __forceinline__ void skip(int m) {
-    for (int j = 0; j < m; ++j) next();
-  }
-};
+using namespace att;
+using Ring = RingPos<kRing>;
 
 __global__ void __launch_bounds__(224, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmV,
@@ -266,7 +122,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     // blocks of tile i (i < n) followed by the value slabs of tile i-1
     // (i >= 1), the order in which the MMA warp consumes them.
     const bool leader = tc::elect_one();
-    RingPos rp;   // next stage to fill
+    Ring rp;   // next stage to fill
     SegIter it;
     it.init(&a, c, t);
     int sb, p0, p1, slot, k = 0;
@@ -283,15 +139,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
         for (int fb = 0; fb < 9; ++fb)
           tc::bulk_load(sQ + fb * 16384, qsrc + fb * 16384, 16384, smem_u32(q_full));
       }
+      TilePages cur, prev;   // tile i (score blocks) and tile i-1 (value slabs)
+      cur.load(a, sb, p0, p1);
       for (int i = 0; ok && i <= n; ++i) {
         const int nsc = i < n ? 9 : 0;
         const int tv = p0 + (i - 1) * kTile;   // tile whose value slabs follow
         const int nv = i >= 1 ? nslabs_of(tv, p1) : 0;
+        TilePages nxt;
+        if (i + 1 < n) nxt.load(a, sb, p0 + (i + 1) * kTile, p1);   // used next step
         int y0 = 0, y1 = 0;
         if (nsc) {
-          const int ts = p0 + i * kTile;
-          y0 = page_row(a, sb, ts);
-          y1 = ts + kPage < p1 ? page_row(a, sb, ts + kPage) : oob_row;
+          y0 = cur.row(a, 0, sb, oob_row);
+          y1 = cur.row(a, 1, sb, oob_row);
         }
         for (int j = 0; j < nsc + nv; ++j, rp.next()) {
           const int s = rp.s;
@@ -305,8 +164,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           const uint32_t dst = sR + s * kStage;
           int y = 0;
           if (j >= nsc) {
-            const int pv = tv + 32 * (j - nsc);
-            y = page_row(a, sb, pv) + (pv % kPage);
+            const int v = j - nsc;   // slab: page v / 2 of tile i-1, rows (v % 2) * 32..
+            y = prev.row(a, v >> 1, sb, oob_row) + (v & 1) * 32;
           }
           issued = rp.n + 1;
           if (leader) {
@@ -321,6 +180,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             }
           }
         }
+        prev = cur;
+        cur = nxt;
       }
       ++k;
     }
@@ -336,7 +197,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     // descriptors at offset 0; a K step adds (byte offset / 16)
     const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
     const uint64_t dR = tc::sdesc(sR, 16, 1024);
-    RingPos rp;   // next stage in ring order
+    Ring rp;   // next stage in ring order
     int g = 0, k = 0;
     bool ok = true;
     SegIter it;
@@ -388,7 +249,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     const bool leader = tc::elect_one();
     constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
     const uint64_t dV = tc::sdesc(sR, 4096, 1024);   // value slab: MN-major
-    RingPos rp;
+    Ring rp;
     int g = 0, k = 0;
     bool ok = true;
     SegIter it;
@@ -423,7 +284,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             tc::fence_after_sync();
             const int vis = p1 - (tv + 32 * v);
             if (vis < 32) {
-              zero_stale_rows(smem + kOffRing + s * kStage, vis, lane);
+              zero_stale_rows<4>(smem + kOffRing + s * kStage, vis, lane);
               __syncwarp();
             }
             if (leader) {
@@ -447,88 +308,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
     if (leader) tc::mma_commit(smem_u32(drained));
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ softmax warps
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;          // head
-    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    SegIter it;
-    it.init(&a, c, t);
-    int sb, p0, p1, slot, g = 0;
-    bool ok = true;
-    while (ok && it.next(&sb, &p0, &p1, &slot)) {
-      const int n = ntiles_of(p0, p1);
-      const size_t prow = ((size_t)slot * a.T + t) * kHeads + row;
-      float* dst = a.part_o + prow * kLat + half * 256;
-      if (n == 0) {
-        for (int j = 0; j < 256; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (half == 0) a.part_lse[prow] = -INFINITY;
-        continue;
-      }
-      float m_used = -INFINITY, l = 0.f;
-      for (int i = 0; i < n; ++i, ++g) {
-        const uint32_t scol = trow + kColS + (g & 1) * kTile;
-        ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, a.status, 27);
-        if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
-        tc::fence_after_sync();
-        const int valid = min(kTile, p1 - (p0 + i * kTile));
-        // the whole S row of this tile (128 tokens) into registers
-        uint32_t lo[64], hi[64];
-        tc::tmem_ld64(scol, lo);
-        tc::tmem_ld64(scol + 64, hi);
-        float mx = valid == kTile ? row_max<false>(lo, hi, valid) : row_max<true>(lo, hi, valid);
-        mx *= a.scale_log2;
-        // S(g) done implies every earlier value MMA but PV(g-1) is done, so
-        // P(g) may overwrite S(g) now; only a rescale of O waits for PV(g-1).
-        const bool need = mx > m_used + kRescale;
-        if (i == 0) {
-          m_used = mx;
-        } else if (__any_sync(0xffffffffu, need)) {
-          ok = mbar_wait(pv_done + 6 * ((g - 1) & 1), ((g - 1) >> 1) & 1, a.status, 28);
-          if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-          tc::fence_after_sync();
-          const float m_new = need ? mx : m_used;
-          const float f = exp2f(m_used - m_new);
-          l *= f;
-          for (int c0 = 0; c0 < 256; c0 += 16) {
-            float v[16];
-            tc::tmem_ld16(trow + c0, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= f;
-            tc::tmem_st16(trow + c0, v);
-          }
-          m_used = m_new;
-        }
-        // P = 2^(s*scale - m) as bf16, packed two per column over the S
-        // columns (tokens 2j, 2j+1 -> column j)
-        uint32_t pk[64];
-        const float psum = valid == kTile
-                               ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
-                               : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
-        tc::tmem_st64(scol, pk);
-        l += psum;
-        tc::fence_before_sync();
-        tc::mbar_arrive(smem_u32(p_full + 6 * (g & 1)));
-      }
-      if (!ok) break;
-      // segment epilogue: O / l and the log-sum-exp
-      // PV of the last tile done implies every earlier one is
-      ok = mbar_wait(pv_done + 6 * ((g - 1) & 1), ((g - 1) >> 1) & 1, a.status, 29);
-      if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-      tc::fence_after_sync();
-      const float inv = 1.f / l;
-      for (int c0 = 0; c0 < 256; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(trow + c0, v);
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          __stcg(reinterpret_cast<float4*>(dst + c0 + j),
-                 make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
-      }
-      if (half == 0) a.part_lse[prow] = m_used + log2f(l);
-      tc::fence_before_sync();
-      tc::mbar_arrive(smem_u32(o_free));
-    }
-    if (!ok) *abort_flag = 1;
+    softmax_role<false>(a, tmem, warp, lane, c, t, t, half, &s_full[0], &s_full[1], pv_done,
+                        pv_done + 6, abort_flag,
+                        [&](int g) { tc::mbar_arrive(smem_u32(p_full + 6 * (g & 1))); },
+                        [&] { tc::mbar_arrive(smem_u32(o_free)); });
   }
 
   // ------------------------------------------------------------ teardown

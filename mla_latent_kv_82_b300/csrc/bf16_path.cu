@@ -243,7 +243,10 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
   }
   // ---- split-KV attention over the latent cache
-  if (!tc_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) return false;
+  const bool paired = T % 2 == 0;   // tokens 2j, 2j+1 share every cache tile
+  if (!(paired ? tc_attend_pair : tc_attend)(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws,
+                                             L, st))
+    return false;
   // ---- log-sum-exp combine -> o_lat (bf16)
   {
     prof_mark(ctx, st, "combine");

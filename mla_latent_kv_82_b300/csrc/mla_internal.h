@@ -85,6 +85,11 @@ size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M);
 bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
                int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
                const WsLayout& L, cudaStream_t st);
+// Same contract for an even T: query tokens 2j, 2j+1 share each cache tile on a
+// CTA pair (cta_group::2).
+bool tc_attend_pair(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
+               int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
+               const WsLayout& L, cudaStream_t st);
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
 

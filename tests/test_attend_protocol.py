@@ -231,3 +231,381 @@ def test_model_catches_lap_aliasing():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+# ---------------------------------------------------------------------------
+# Paired kernel (even T): a cluster of two CTAs, one per query token, shares
+# every cache tile.  The even CTA issues all MMAs with cta_group::2; each CTA
+# loads its half of each stage into its own 10-slot ring, and both halves
+# complete the even CTA's `ready` barrier (modelled as one arrival per CTA).
+# A value slab past the visible end is the exception: the odd CTA loads it
+# against a local barrier and its relay warp completes it on `ready` after
+# zeroing stale rows; the relay also forwards the odd CTA's query image.
+# Commits reach both CTAs (multicast); the softmax warps of both CTAs arrive
+# on the even CTA's p_full and o_free.  Ring step i of a segment holds score
+# blocks 0-4 of tile i, the value slabs of tile i-1, then score blocks 5-8 of
+# tile i, so PV(i-1) overlaps S(i).
+
+PRING = 10
+
+
+def step_items(i, n, nv_prev):
+    """('S', b) / ('V', v) items of ring step i (i = 0..n) in ring order."""
+    nsc = 9 if i < n else 0
+    head = 5 if nsc else 0
+    out = [("S", b) for b in range(head)]
+    out += [("V", v) for v in range(nv_prev if i >= 1 else 0)]
+    out += [("S", b) for b in range(head, nsc)]
+    return out
+
+
+class Ring10(Ring):
+    def next(self):
+        self.n += 1
+        self.s = (self.s + 1) % PRING
+
+
+def run_pair_protocol(segs, rescale: bool, seed: int | None, seg_guard: bool = True):
+    """seg_guard: the score role waits for PV of the previous tile before the
+    first tile of a later segment."""
+    rnd = random.Random(seed)
+    ready = [Bar(f"ready{i}", 2) for i in range(PRING)]
+    zb = Bar("zb")
+    empty = {r: [Bar(f"empty{r}{i}") for i in range(PRING)] for r in "LP"}
+    s_full = {r: [Bar(f"s_full{r}0"), Bar(f"s_full{r}1")] for r in "LP"}
+    pv_done = {r: [Bar(f"pv_done{r}0"), Bar(f"pv_done{r}1")] for r in "LP"}
+    q_empty = {r: Bar(f"q_empty{r}") for r in "LP"}
+    p_full = [Bar("p_full0", 2), Bar("p_full1", 2)]
+    q_ready, q_full_p, o_free = Bar("q_ready", 2), Bar("q_fullP"), Bar("o_free", 2)
+
+    def steps(n, p0, p1):
+        for i in range(n + 1):
+            yield i, step_items(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
+
+    def partial(i, item, p0, p1):
+        kind, v = item
+        return kind == "V" and p1 - (p0 + (i - 1) * TILE + 32 * v) < 32
+
+    def producer(side):
+        rp, k = Ring10(), 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            if k > 0:
+                yield q_empty[side], k - 1
+            (q_ready if side == "L" else q_full_p).arrive()
+            for i, items in steps(n, p0, p1):
+                for item in items:
+                    if rp.n >= PRING:
+                        yield empty[side][rp.s], rp.n // PRING - 1
+                    if side == "P" and partial(i, item, p0, p1):
+                        zb.arrive()
+                    else:
+                        ready[rp.s].arrive()
+                    rp.next()
+            k += 1
+
+    def relay():
+        rp, k, nz = Ring10(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            yield q_full_p, k
+            q_ready.arrive()
+            for i, items in steps(n, p0, p1):
+                for item in items:
+                    if partial(i, item, p0, p1):
+                        yield zb, nz
+                        ready[rp.s].arrive()
+                        nz += 1
+                    rp.next()
+            k += 1
+
+    def both(bars):
+        for b in bars:
+            b.arrive()
+
+    def score_mma():
+        rp, g, k = Ring10(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            yield q_ready, k
+            for i, items in steps(n, p0, p1):
+                gs = g + i
+                if i < n:
+                    if gs >= 2:
+                        yield pv_done["L"][gs & 1], (gs - 2) >> 1
+                    if seg_guard and i == 0 and gs >= 1:
+                        yield pv_done["L"][(gs - 1) & 1], (gs - 1) >> 1
+                for kind, _ in items:
+                    if kind == "S":
+                        yield ready[rp.s], rp.n // PRING
+                        both([empty["L"][rp.s], empty["P"][rp.s]])
+                    rp.next()
+                if i < n:
+                    both([s_full["L"][gs & 1], s_full["P"][gs & 1]])
+                    if i == n - 1:
+                        both([q_empty["L"], q_empty["P"]])
+            g += n
+            k += 1
+
+    def value_mma():
+        rp, g, k = Ring10(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            for i, items in steps(n, p0, p1):
+                gv = g + i - 1
+                if i >= 1:
+                    if i == 1 and k > 0:
+                        yield o_free, k - 1
+                    yield p_full[gv & 1], gv >> 1
+                for kind, _ in items:
+                    if kind == "V":
+                        yield ready[rp.s], rp.n // PRING
+                        both([empty["L"][rp.s], empty["P"][rp.s]])
+                    rp.next()
+                if i >= 1:
+                    both([pv_done["L"][gv & 1], pv_done["P"][gv & 1]])
+            g += n
+            k += 1
+
+    def softmax(side):
+        g = 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            for i in range(n):
+                yield s_full[side][g & 1], g >> 1
+                if i > 0 and rescale:
+                    yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
+                p_full[g & 1].arrive()
+                g += 1
+            yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
+            o_free.arrive()
+
+    roles = {"producerL": producer("L"), "producerP": producer("P"), "relay": relay(),
+             "score": score_mma(), "value": value_mma(), "softmaxL": softmax("L"),
+             "softmaxP": softmax("P")}
+    waiting = {r: None for r in roles}
+    alive = list(roles)
+    while alive:
+        cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
+        if not cand:
+            return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
+        r = rnd.choice(cand) if seed is not None else cand[0]
+        try:
+            waiting[r] = next(roles[r])
+        except StopIteration:
+            alive.remove(r)
+            waiting[r] = None
+    return None
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 8, 13])
+def test_pair_single_and_multi_segment(n_tiles):
+    segs = [(0, 0, n_tiles * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200),
+            (5, 0, 2 * TILE), (6, 0, TILE)]
+    for seed in range(16):
+        assert run_pair_protocol(segs, seed % 2 == 0, seed) is None
+
+
+def test_pair_workload_split_plan():
+    for name in ("b128-l16k-t2", "b64-paged"):
+        wl = W.config(name)
+        G = 148 // 4
+        plans = split_segments(wl.seq_lens, 2, 1, G)
+        for c, segs in enumerate(plans):
+            if c % 3:
+                continue
+            for rescale, seed in ((False, None), (True, 5)):
+                assert run_pair_protocol(segs, rescale, seed) is None, (name, c)
+
+
+# Paired kernel, 16 KB stages: a stage carries two score blocks (or the last
+# one) or two value slabs (or the last one) of this CTA's half, in a 5-slot
+# ring.  Ring step i: score stages {0,1}, {2,3}, the value stages of tile
+# i-1, then score stages {4,5}, {6,7}, {8}.
+
+PRING2 = 5
+
+
+def step_items2(i, n, nv_prev):
+    """('S', first block) / ('V', first slab) stages of ring step i."""
+    score = [("S", b) for b in (0, 2, 4, 6, 8)] if i < n else []
+    vals = [("V", v) for v in range(0, nv_prev, 2)] if i >= 1 else []
+    return score[:2] + vals + score[2:] if score else vals
+
+
+class Ring5(Ring):
+    pass
+
+
+def run_pair16_protocol(segs, rescale: bool, seed: int | None):
+    rnd = random.Random(seed)
+    R = PRING2
+    ready = [Bar(f"ready{i}", 2) for i in range(R)]
+    zb = Bar("zb")
+    empty = {r: [Bar(f"empty{r}{i}") for i in range(R)] for r in "LP"}
+    s_full = {r: [Bar(f"s_full{r}0"), Bar(f"s_full{r}1")] for r in "LP"}
+    pv_done = {r: [Bar(f"pv_done{r}0"), Bar(f"pv_done{r}1")] for r in "LP"}
+    q_empty = {r: Bar(f"q_empty{r}") for r in "LP"}
+    p_full = [Bar("p_full0", 2), Bar("p_full1", 2)]
+    q_ready, q_full_p, o_free = Bar("q_ready", 2), Bar("q_fullP"), Bar("o_free", 2)
+
+    def steps(n, p0, p1):
+        for i in range(n + 1):
+            yield i, step_items2(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
+
+    def partial(i, item, p0, p1):
+        kind, v = item
+        if kind != "V":
+            return False
+        last = min(v + 2, nslabs(p0 + (i - 1) * TILE, p1)) - 1
+        return p1 - (p0 + (i - 1) * TILE + 32 * last) < 32
+
+    def producer(side):
+        rp, k = Ring(), 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            if k > 0:
+                yield q_empty[side], k - 1
+            (q_ready if side == "L" else q_full_p).arrive()
+            for i, items in steps(n, p0, p1):
+                for item in items:
+                    if rp.n >= R:
+                        yield empty[side][rp.s], rp.n // R - 1
+                    if side == "P" and partial(i, item, p0, p1):
+                        zb.arrive()
+                    else:
+                        ready[rp.s].arrive()
+                    rp.next()
+            k += 1
+
+    def relay():
+        rp, k, nz = Ring(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            yield q_full_p, k
+            q_ready.arrive()
+            for i, items in steps(n, p0, p1):
+                for item in items:
+                    if partial(i, item, p0, p1):
+                        yield zb, nz
+                        ready[rp.s].arrive()
+                        nz += 1
+                    rp.next()
+            k += 1
+
+    def both(bars):
+        for b in bars:
+            b.arrive()
+
+    def score_mma():
+        rp, g, k = Ring(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            yield q_ready, k
+            for i, items in steps(n, p0, p1):
+                gs = g + i
+                if i < n:
+                    if gs >= 2:
+                        yield pv_done["L"][gs & 1], (gs - 2) >> 1
+                    if i == 0 and gs >= 1:
+                        yield pv_done["L"][(gs - 1) & 1], (gs - 1) >> 1
+                for kind, _ in items:
+                    if kind == "S":
+                        yield ready[rp.s], rp.n // R
+                        both([empty["L"][rp.s], empty["P"][rp.s]])
+                    rp.next()
+                if i < n:
+                    both([s_full["L"][gs & 1], s_full["P"][gs & 1]])
+                    if i == n - 1:
+                        both([q_empty["L"], q_empty["P"]])
+            g += n
+            k += 1
+
+    def value_mma():
+        rp, g, k = Ring(), 0, 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            for i, items in steps(n, p0, p1):
+                gv = g + i - 1
+                if i >= 1:
+                    if i == 1 and k > 0:
+                        yield o_free, k - 1
+                    yield p_full[gv & 1], gv >> 1
+                for kind, _ in items:
+                    if kind == "V":
+                        yield ready[rp.s], rp.n // R
+                        both([empty["L"][rp.s], empty["P"][rp.s]])
+                    rp.next()
+                if i >= 1:
+                    both([pv_done["L"][gv & 1], pv_done["P"][gv & 1]])
+            g += n
+            k += 1
+
+    def softmax(side):
+        g = 0
+        for _, p0, p1 in segs:
+            n = ntiles(p0, p1)
+            if n == 0:
+                continue
+            for i in range(n):
+                yield s_full[side][g & 1], g >> 1
+                if i > 0 and rescale:
+                    yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
+                p_full[g & 1].arrive()
+                g += 1
+            yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
+            o_free.arrive()
+
+    roles = {"producerL": producer("L"), "producerP": producer("P"), "relay": relay(),
+             "score": score_mma(), "value": value_mma(), "softmaxL": softmax("L"),
+             "softmaxP": softmax("P")}
+    waiting = {r: None for r in roles}
+    alive = list(roles)
+    while alive:
+        cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
+        if not cand:
+            return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
+        r = rnd.choice(cand) if seed is not None else cand[0]
+        try:
+            waiting[r] = next(roles[r])
+        except StopIteration:
+            alive.remove(r)
+            waiting[r] = None
+    return None
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 8, 13])
+def test_pair16_single_and_multi_segment(n_tiles):
+    segs = [(0, 0, n_tiles * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200),
+            (5, 0, 2 * TILE), (6, 0, TILE), (7, 0, 100)]
+    for seed in range(16):
+        assert run_pair16_protocol(segs, seed % 2 == 0, seed) is None
+
+
+def test_pair16_workload_split_plan():
+    for name in ("b128-l16k-t2", "b64-paged"):
+        wl = W.config(name)
+        plans = split_segments(wl.seq_lens, 2, 1, 148 // 4)
+        for c, segs in enumerate(plans):
+            if c % 3:
+                continue
+            for rescale, seed in ((False, None), (True, 5)):
+                assert run_pair16_protocol(segs, rescale, seed) is None, (name, c)
