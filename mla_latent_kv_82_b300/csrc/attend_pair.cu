@@ -81,7 +81,10 @@ __device__ __forceinline__ int step_stages(bool sc, int nv) { return (sc ? 5 : 0
 
 __global__ void __launch_bounds__(256, 1)
 attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
-                   const __grid_constant__ CUtensorMap tmV, const AttArgs a) {
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmS2,   // two score blocks
+                   const __grid_constant__ CUtensorMap tmV2,   // two value slabs
+                   const AttArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -135,6 +138,8 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
   if (warp == 0 && lane == 0) {
     tc::prefetch_tmap(&tmS);
     tc::prefetch_tmap(&tmV);
+    tc::prefetch_tmap(&tmS2);
+    tc::prefetch_tmap(&tmV2);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -218,20 +223,29 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
             if (even) tc::mbar_arrive_expect_tx(fb, 2 * bytes);   // both CTAs' halves
             if (!even && partial) tc::mbar_arrive_expect_tx(smem_u32(zb), bytes);
             const uint32_t eb = even_bar(&ring[s]);
-            for (int u = 0; u < cnt; ++u) {
-              if (first >= 0) {
-                const int x = (first + u) * 64;
-                if (even) tc::tma_load_2d(dst + u * kPHalf, &tmS, x, ys, fb);
-                else tc::tma_load_2d_pair(dst + u * kPHalf, &tmS, x, ys, eb);
-              } else {
+            const uint32_t zbb = smem_u32(zb);
+            const int vb = half * 4 + (int)rank * 2;   // this CTA's value column blocks
+            if (cnt == 2 && first >= 0) {
+              // both blocks in one copy ([2][64 rows][64])
+              if (even) tc::tma_load_3d(dst, &tmS2, 0, ys, first, fb);
+              else tc::tma_load_3d_pair(dst, &tmS2, 0, ys, first, eb);
+            } else if (cnt == 2) {
+              // both slabs (one page, 64 rows) in one copy ([2][2 blocks][32][64])
+              const int slab = y[0] / 32;
+              if (even) tc::tma_load_4d(dst, &tmV2, 0, 0, vb, slab, fb);
+              else if (partial) tc::tma_load_4d(dst, &tmV2, 0, 0, vb, slab, zbb);
+              else tc::tma_load_4d_pair(dst, &tmV2, 0, 0, vb, slab, eb);
+            } else if (first >= 0) {
+              if (even) tc::tma_load_2d(dst, &tmS, first * 64, ys, fb);
+              else tc::tma_load_2d_pair(dst, &tmS, first * 64, ys, eb);
+            } else {
 #pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                  const uint32_t d = dst + u * kPHalf + f * 4096;
-                  const int x = half * 256 + (int)rank * 128 + f * 64;
-                  if (even) tc::tma_load_2d(d, &tmV, x, y[u], fb);
-                  else if (partial) tc::tma_load_2d(d, &tmV, x, y[u], smem_u32(zb));
-                  else tc::tma_load_2d_pair(d, &tmV, x, y[u], eb);
-                }
+              for (int f = 0; f < 2; ++f) {
+                const uint32_t d = dst + f * 4096;
+                const int x = (vb + f) * 64;
+                if (even) tc::tma_load_2d(d, &tmV, x, y[0], fb);
+                else if (partial) tc::tma_load_2d(d, &tmV, x, y[0], zbb);
+                else tc::tma_load_2d_pair(d, &tmV, x, y[0], eb);
               }
             }
           }
@@ -471,9 +485,11 @@ bool tc_attend_pair(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16
                     int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
                     const WsLayout& L, cudaStream_t st) {
   if (T % 2 != 0) return false;
-  CUtensorMap tmS, tmV;
-  if (!make_tmap_bf16_2d(&tmS, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 64, false) ||
-      !make_tmap_bf16_2d(&tmV, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 32, false))
+  CUtensorMap tmS, tmV, tmS2, tmV2;
+  const uint64_t rows = (uint64_t)num_pages * kPage;
+  if (!make_tmap_bf16_2d(&tmS, cache, rows, kRow, kRow, 64, 64, false) ||
+      !make_tmap_bf16_2d(&tmV, cache, rows, kRow, kRow, 64, 32, false) ||
+      !make_tmap_pool_blocks(&tmS2, cache, rows, 64, 2) || !make_tmap_pool_slabs(&tmV2, cache, rows, 2))
     return false;
   AttArgs a{};
   a.lens = reinterpret_cast<const int*>(ws + L.lens);
@@ -515,7 +531,7 @@ bool tc_attend_pair(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16
   cfg.numAttrs = 2;
   prof_mark(ctx, st, "attend");
   ctx->launches += 1;
-  return cudaLaunchKernelEx(&cfg, attend_pair_kernel, tmS, tmV, a) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, attend_pair_kernel, tmS, tmV, tmS2, tmV2, a) == cudaSuccess;
 }
 
 }  // namespace mla

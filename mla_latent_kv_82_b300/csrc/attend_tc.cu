@@ -174,9 +174,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
               tc::tma_load_2d(dst, &tmS, j * 64, y0, fb);
               tc::tma_load_2d(dst + 8192, &tmS, j * 64, y1, fb);
             } else {
-#pragma unroll
-              for (int f = 0; f < 4; ++f)
-                tc::tma_load_2d(dst + f * 4096, &tmV, half * 256 + f * 64, y, fb);
+              // the slab's 4 column blocks of this half in one copy ([4][32][64])
+              tc::tma_load_3d(dst, &tmV, 0, y, half * 4, fb);
             }
           }
         }
@@ -339,8 +338,9 @@ bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
                int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
                const WsLayout& L, cudaStream_t st) {
   CUtensorMap tmS, tmV;
-  if (!make_tmap_bf16_2d(&tmS, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 64, false) ||
-      !make_tmap_bf16_2d(&tmV, cache, (uint64_t)num_pages * kPage, kRow, kRow, 64, 32, false))
+  const uint64_t rows = (uint64_t)num_pages * kPage;
+  if (!make_tmap_bf16_2d(&tmS, cache, rows, kRow, kRow, 64, 64, false) ||
+      !make_tmap_pool_blocks(&tmV, cache, rows, 32, 4))
     return false;
   AttArgs a{};
   a.lens = reinterpret_cast<const int*>(ws + L.lens);

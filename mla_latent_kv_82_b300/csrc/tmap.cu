@@ -39,4 +39,29 @@ bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_
   return r == CUDA_SUCCESS;
 }
 
+static bool encode_pool(CUtensorMap* tm, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                        const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_pool_blocks(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows,
+                           uint32_t nb) {
+  const cuuint64_t dims[3] = {64, rows, 9};
+  const cuuint64_t strides[2] = {1152, 128};
+  const cuuint32_t box[3] = {64, box_rows, nb};
+  return encode_pool(tm, base, 3, dims, strides, box);
+}
+
+bool make_tmap_pool_slabs(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t nb) {
+  const cuuint64_t dims[4] = {64, 32, 9, rows / 32};
+  const cuuint64_t strides[3] = {1152, 128, 32 * 1152};
+  const cuuint32_t box[4] = {64, 32, nb, 2};
+  return encode_pool(tm, base, 4, dims, strides, box);
+}
+
 }  // namespace mla

@@ -13,4 +13,16 @@ namespace mla {
 bool make_tmap_bf16_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t ld_elems, uint32_t box_cols, uint32_t box_rows, bool weights);
 
+// Views of the latent cache pool [rows, 576] bf16 (row stride 1152 bytes)
+// that let one copy fetch several 64-column blocks, each landing as its own
+// 128-byte-swizzled block in shared memory (block after block):
+//   blocks: dims {64 columns, rows, 9 blocks}, box {64, box_rows, nb} ->
+//           [nb][box_rows][64]; coordinates (0, row, first block);
+//   slabs:  dims {64 columns, 32 rows, 9 blocks, rows / 32 slabs},
+//           box {64, 32, nb, 2} -> [2 slabs][nb][32][64]; coordinates
+//           (0, 0, first block, first slab).
+bool make_tmap_pool_blocks(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t box_rows,
+                           uint32_t nb);
+bool make_tmap_pool_slabs(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t nb);
+
 }  // namespace mla
