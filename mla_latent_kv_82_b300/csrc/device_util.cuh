@@ -77,10 +77,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   return false;
 }
 
-// Wait on a barrier that other CTAs of the cluster arrive on (remote arrive
-// or multicast commit): acquire at cluster scope, and poll with the
-// non-blocking probe, since a suspended try_wait is not reliably woken early
-// by a remote arrival.  Bounded like mbar_wait.
+// Wait on a barrier that other CTAs of the cluster arrive on (remote arrive,
+// multicast commit, or a copy issued by the other CTA): acquire at cluster
+// scope.  Bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -93,15 +92,26 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t p
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status,
                                                   int where, uint64_t max_ns = 2000000000ull) {
   if (mbar_test_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (long long i = 1;; ++i) {
-    // back off between probes: a tight loop of barrier probes competes with
-    // the tensor cores' operand reads for shared-memory bandwidth
-    __nanosleep(32);
-    if (mbar_test_wait_cluster(bar, parity)) return true;
+    // the potentially blocking probe suspends the thread in hardware until
+    // the phase completes or a time limit passes
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 255) == 0 && global_ns() - t0 > max_ns) break;
   }
   report(status, MLA_ERR_TIMEOUT, where);

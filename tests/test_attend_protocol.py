@@ -92,8 +92,10 @@ def split_segments(seq_lens, T, t, G):
 
 def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
     """Returns None when every role finishes, else the blocked roles.
-    `guard` = False drops the value-MMA role's wait for S(x+1)."""
+    `guard` = False drops the value-MMA role's wait for S(x+1).  Issued
+    copies complete in random order (a separate copy-engine role)."""
     rnd = random.Random(seed)
+    pending = []
     full = [Bar(f"full{i}") for i in range(RING)]
     empty = [Bar(f"empty{i}") for i in range(RING)]
     s_full = [Bar("s_full0"), Bar("s_full1")]
@@ -116,7 +118,7 @@ def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
                 for _ in range(nsc + nv):
                     if rp.n >= RING:
                         yield empty[rp.s], rp.n // RING - 1
-                    full[rp.s].arrive()
+                    pending.append(full[rp.s])
                     rp.next()
             k += 1
 
@@ -189,6 +191,9 @@ def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
     alive = list(roles)
     while alive:
         cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
+        if pending and (not cand or rnd.random() < 0.5):
+            pending.pop(rnd.randrange(len(pending))).arrive()
+            continue
         if not cand:
             return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
         r = rnd.choice(cand) if seed is not None else cand[0]
@@ -447,8 +452,14 @@ class Ring5(Ring):
     pass
 
 
-def run_pair16_protocol(segs, rescale: bool, seed: int | None):
+def run_pair16_protocol(segs, rescale: bool, seed: int | None, items_fn=None,
+                        slabs_per_stage: int = 2, in_order: bool = False):
+    """items_fn / slabs_per_stage: the step layout (default: two slabs per
+    value stage, step_items2).  Issued copies complete in random order (a
+    separate copy-engine role), unless in_order."""
+    items_fn = items_fn or step_items2
     rnd = random.Random(seed)
+    pending = []   # barriers of issued, not yet completed copies
     R = PRING2
     ready = [Bar(f"ready{i}", 2) for i in range(R)]
     zb = Bar("zb")
@@ -461,13 +472,13 @@ def run_pair16_protocol(segs, rescale: bool, seed: int | None):
 
     def steps(n, p0, p1):
         for i in range(n + 1):
-            yield i, step_items2(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
+            yield i, items_fn(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
 
     def partial(i, item, p0, p1):
         kind, v = item
         if kind != "V":
             return False
-        last = min(v + 2, nslabs(p0 + (i - 1) * TILE, p1)) - 1
+        last = min(v + slabs_per_stage, nslabs(p0 + (i - 1) * TILE, p1)) - 1
         return p1 - (p0 + (i - 1) * TILE + 32 * last) < 32
 
     def producer(side):
@@ -484,11 +495,19 @@ def run_pair16_protocol(segs, rescale: bool, seed: int | None):
                     if rp.n >= R:
                         yield empty[side][rp.s], rp.n // R - 1
                     if side == "P" and partial(i, item, p0, p1):
-                        zb.arrive()
+                        pending.append(zb)
                     else:
-                        ready[rp.s].arrive()
+                        pending.append(ready[rp.s])
+                    if in_order:
+                        pending.pop(0).arrive()
                     rp.next()
             k += 1
+
+    def copy_engine():
+        while True:
+            if pending:
+                pending.pop(rnd.randrange(len(pending))).arrive()
+            yield None
 
     def relay():
         rp, k, nz = Ring(), 0, 0
@@ -577,10 +596,14 @@ def run_pair16_protocol(segs, rescale: bool, seed: int | None):
     roles = {"producerL": producer("L"), "producerP": producer("P"), "relay": relay(),
              "score": score_mma(), "value": value_mma(), "softmaxL": softmax("L"),
              "softmaxP": softmax("P")}
+    engine = copy_engine()
     waiting = {r: None for r in roles}
     alive = list(roles)
     while alive:
         cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
+        if pending and (not cand or rnd.random() < 0.5):
+            next(engine)
+            continue
         if not cand:
             return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
         r = rnd.choice(cand) if seed is not None else cand[0]
@@ -609,3 +632,28 @@ def test_pair16_workload_split_plan():
                 continue
             for rescale, seed in ((False, None), (True, 5)):
                 assert run_pair16_protocol(segs, rescale, seed) is None, (name, c)
+
+
+# A ring order that is unsafe when copies complete out of order: value slabs
+# all between score stages {2,3} and {4,5} with one slab per stage.  The
+# last slab's slot was last used by this step's first score stage, which
+# the value role's waits do not cover.
+
+def step_items_unsafe(i, n, nv_prev):
+    score = [("S", b) for b in (0, 2, 4, 6, 8)] if i < n else []
+    vals = [("V", v) for v in range(nv_prev)] if i >= 1 else []
+    return score[:2] + vals + score[2:] if score else vals
+
+
+def test_model_catches_out_of_order_hazard():
+    """With step_items_unsafe a slow copy lets the value role pass a parity
+    wait a lap early: the model, whose copies complete in random order,
+    reports it."""
+    failures = 0
+    for seed in range(60):
+        try:
+            failures += run_pair16_protocol([(0, 0, 6 * TILE)], False, seed,
+                                            step_items_unsafe, 1) is not None
+        except AssertionError:
+            failures += 1
+    assert failures > 0
