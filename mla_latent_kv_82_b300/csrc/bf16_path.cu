@@ -17,10 +17,94 @@ namespace {
 
 // Merge the split partials of one (token, head) into o_lat = sum_s w_s O_s /
 // sum_s w_s with w_s = 2^(lse_s - max lse): the log-sum-exp combine of
-// flash-decoding.  One thread per (token, head, 4 latent columns); the
-// partial rows are read as coalesced float4 runs.
+// flash-decoding.  For sequences cut into many splits (a few long
+// sequences), one CTA per (token, head): the split weights are formed
+// once in shared memory, then two groups of 128 threads (one float4 of the
+// 512 latent columns per thread) each sum every other split with eight
+// independent loads in flight, and the two sums are added in a fixed order.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxSlots = 1024;
+
+__global__ void __launch_bounds__(kCombineThreads)
+combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                     const int* __restrict__ slot_base, int T, __nv_bfloat16* __restrict__ o_lat,
+                     int* status) {
+  __shared__ float w[kCombineMaxSlots];
+  __shared__ float red[2];
+  __shared__ float4 acc1[kLat / 4];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int mh = blockIdx.x;                   // token row * kHeads + head
+  const int m = mh / kHeads, head = mh % kHeads;
+  const int b = m / T, t = m % T;
+  const int s0 = slot_base[b];
+  int n = slot_base[b + 1] - s0;
+  if (n > kCombineMaxSlots) {   // cannot happen with the planner's slot counts
+    if (threadIdx.x == 0) report(status, MLA_ERR_INVALID_ARG, 60);
+    n = kCombineMaxSlots;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // weights: w_s = 2^(lse_s - max); empty splits have lse = -inf, weight 0
+  float lmax = -INFINITY;
+  for (int i = tid; i < n; i += kCombineThreads) {
+    const float v = part_lse[((size_t)(s0 + i) * T + t) * kHeads + head];
+    w[i] = v;
+    lmax = fmaxf(lmax, v);
+  }
+  for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  __shared__ float wmax[kCombineThreads / 32];
+  if (lane == 0) wmax[warp] = lmax;
+  __syncthreads();
+  lmax = wmax[0];
+#pragma unroll
+  for (int i = 1; i < kCombineThreads / 32; ++i) lmax = fmaxf(lmax, wmax[i]);
+  for (int i = tid; i < n; i += kCombineThreads) w[i] = exp2f(w[i] - lmax);
+  __syncthreads();
+  if (tid == 0) {
+    float sum = 0.f;
+    for (int i = 0; i < n; ++i) sum += w[i];
+    red[0] = sum;
+  }
+  const int g = tid >> 7, q4 = tid & 127;
+  const float4* src = reinterpret_cast<const float4*>(part_o) + q4;
+  const size_t stride = (size_t)T * kHeads * (kLat / 4);   // float4s between slots
+  const size_t base = ((size_t)s0 * T + t) * kHeads * (kLat / 4) + (size_t)head * (kLat / 4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = g; i0 < n; i0 += 16) {
+    float4 x[8];
+    float ws[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + 2 * j;
+      ws[j] = i < n ? w[i] : 0.f;
+      x[j] = ws[j] != 0.f ? __ldcg(src + base + (size_t)i * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc.x = fmaf(ws[j], x[j].x, acc.x);
+      acc.y = fmaf(ws[j], x[j].y, acc.y);
+      acc.z = fmaf(ws[j], x[j].z, acc.z);
+      acc.w = fmaf(ws[j], x[j].w, acc.w);
+    }
+  }
+  if (g == 1) acc1[q4] = acc;
+  __syncthreads();
+  if (g == 1) return;
+  const float4 y = acc1[q4];
+  const float inv = 1.f / red[0];
+  const __nv_bfloat162 lo = __floats2bfloat162_rn((acc.x + y.x) * inv, (acc.y + y.y) * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn((acc.z + y.z) * inv, (acc.w + y.w) * inv);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&lo);
+  v.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(o_lat + (size_t)mh * kLat + q4 * 4) = v;
+}
+
+// The same merge with one thread per (token, head, 4 latent columns), for
+// sequences split into a few pieces only (many (token, head) rows, short
+// loops); the partial rows are read as coalesced float4 runs.
 __global__ void __launch_bounds__(256)
-combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+combine_rows_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                const int* __restrict__ slot_base, int T, int M,
                __nv_bfloat16* __restrict__ o_lat) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -251,20 +335,27 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   {
     prof_mark(ctx, st, "combine");
     ctx->launches += 1;
+    // many splits per sequence: a CTA per (token, head); else a thread per
+    // (token, head, 4 columns)
+    const bool per_head = L.n_slots >= 8 * B;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((M * kHeads * (kLat / 4) + 255) / 256);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = per_head ? dim3(M * kHeads) : dim3((M * kHeads * (kLat / 4) + 255) / 256);
+    cfg.blockDim = per_head ? dim3(kCombineThreads) : dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!check(cudaLaunchKernelEx(&cfg, combine_kernel,
-                                  (const float*)reinterpret_cast<float*>(ws + L.part_o),
-                                  (const float*)reinterpret_cast<float*>(ws + L.part_lse),
-                                  (const int*)reinterpret_cast<int*>(ws + L.slot_base), T, M,
-                                  olat)))
+    const float* part_o = reinterpret_cast<const float*>(ws + L.part_o);
+    const float* part_lse = reinterpret_cast<const float*>(ws + L.part_lse);
+    const int* slot_base = reinterpret_cast<const int*>(ws + L.slot_base);
+    const cudaError_t e =
+        per_head ? cudaLaunchKernelEx(&cfg, combine_heads_kernel, part_o, part_lse, slot_base, T,
+                                      olat, ctx->status)
+                 : cudaLaunchKernelEx(&cfg, combine_rows_kernel, part_o, part_lse, slot_base, T,
+                                      M, olat);
+    if (!check(e))
       return false;
   }
   // ---- value up-projection: o_i = W^UV_i o_lat_i
