@@ -178,7 +178,7 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
       const int n = ntiles_of(p0, p1);
       if (n == 0) continue;
       if (k > 0 && !warp_wait<true>(q_empty, (k - 1) & 1, a.status, 41)) { ok = false; break; }
-      if (*abort_flag) { ok = false; break; }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       ++q_issued;
       if (leader) {
         tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
@@ -203,7 +203,7 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
             ok = false;
             break;
           }
-          if (*abort_flag) { ok = false; break; }
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
           int cnt;
           const int first = step_stage(j, sc, nv, &cnt);
           const uint32_t fb = smem_u32(&ring[s]);
@@ -349,7 +349,7 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
           // P(gv) written means S(gv) is done, so every slot this step's
           // slabs reuse has been consumed in its previous lap
           if (!warp_wait<true>(&p_full[gv & 1], (gv >> 1) & 1, a.status, 49)) { ok = false; break; }
-          if (*abort_flag) { ok = false; break; }
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
           tc::fence_after_sync();
         }
         const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
@@ -417,7 +417,7 @@ attend_pair_kernel(const __grid_constant__ CUtensorMap tmS,
           const int vis = p1 - (tv + 32 * (-1 - first + cnt - 1));
           if (vis >= 32) continue;
           if (!warp_wait<true>(zb, nz & 1, a.status, 44)) { ok = false; break; }
-          if (*abort_flag) { ok = false; break; }
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
           zero_stale_rows<2>(smem + kPOffRing + rp.s * kPStage + (cnt - 1) * kPHalf, vis, lane);
           __syncwarp();
           if (leader) {

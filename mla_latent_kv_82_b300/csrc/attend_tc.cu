@@ -131,7 +131,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
       const int n = ntiles_of(p0, p1);
       if (n == 0) continue;
       if (k > 0 && !warp_wait(q_empty, (k - 1) & 1, a.status, 21)) { ok = false; break; }
-      if (*abort_flag) { ok = false; break; }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       ++q_issued;
       if (leader) {
         tc::mbar_arrive_expect_tx(smem_u32(q_full), kQImgBytes);
@@ -159,7 +159,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             ok = false;
             break;
           }
-          if (*abort_flag) { ok = false; break; }
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
           const uint32_t fb = smem_u32(&full[s]);
           const uint32_t dst = sR + s * kStage;
           int y = 0;
@@ -211,6 +211,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
           const int gs = g + i;
           if (gs >= 2 &&
               !warp_wait(pv_done + 6 * (gs & 1), ((gs - 2) >> 1) & 1, a.status, 33)) {
+            ok = false;
+            break;
+          }
+          // A new segment's first score stages follow the previous segment's
+          // last value stages, which this warp stepped over: PV of that tile
+          // must be done, or a slot could still be a lap behind.
+          if (i == 0 && k > 0 &&
+              !warp_wait(pv_done + 6 * ((gs - 1) & 1), ((gs - 1) >> 1) & 1, a.status, 35)) {
             ok = false;
             break;
           }
@@ -273,7 +281,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant_
             ok = false;
             break;
           }
-          if (*abort_flag) { ok = false; break; }
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
           const int ns = nslabs_of(tv, p1);

@@ -90,10 +90,12 @@ def split_segments(seq_lens, T, t, G):
     return out
 
 
-def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
+def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True,
+                 seg_guard: bool = True):
     """Returns None when every role finishes, else the blocked roles.
-    `guard` = False drops the value-MMA role's wait for S(x+1).  Issued
-    copies complete in random order (a separate copy-engine role)."""
+    `guard` = False drops the value-MMA role's wait for S(x+1), `seg_guard`
+    = False the score-MMA role's wait for the previous segment's last PV.
+    Issued copies complete in random order (a separate copy-engine role)."""
     rnd = random.Random(seed)
     pending = []
     full = [Bar(f"full{i}") for i in range(RING)]
@@ -134,6 +136,8 @@ def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
                     gs = g + i
                     if gs >= 2:
                         yield pv_done[gs & 1], (gs - 2) >> 1
+                    if i == 0 and k > 0 and seg_guard:
+                        yield pv_done[(gs - 1) & 1], (gs - 1) >> 1
                     for _ in range(9):
                         yield full[rp.s], rp.n // RING
                         empty[rp.s].arrive()
@@ -185,8 +189,8 @@ def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True):
             yield pv_done[(g - 1) & 1], (g - 1) >> 1
             o_free.arrive()
 
-    roles = {"producer": producer(), "score": score_mma(), "value": value_mma(),
-             "softmax": softmax()}
+    roles = {"score": score_mma(), "value": value_mma(), "softmax": softmax(),
+             "producer": producer()}
     waiting = {r: None for r in roles}
     alive = list(roles)
     while alive:
@@ -223,6 +227,20 @@ def test_workload_split_plans(name):
                 continue   # long splits: every fourth keeps the test short
             for rescale, seed in ((False, None), (True, 7), (False, 11)):
                 assert run_protocol(segs, rescale, seed) is None, (t, c)
+
+
+def test_model_catches_segment_start_aliasing():
+    """Without the score-MMA role's wait for the previous segment's last PV,
+    a one-tile segment followed by another lets that role pass a parity wait
+    on a slot whose value-stage fill of the lap before has not landed."""
+    segs = [(0, 0, TILE), (1, 0, 3 * TILE - 40)]
+    failures = 0
+    for seed in range(40):
+        try:
+            failures += run_protocol(segs, seed % 2 == 0, seed, seg_guard=False) is not None
+        except AssertionError:
+            failures += 1
+    assert failures > 0
 
 
 def test_model_catches_lap_aliasing():
