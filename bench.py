@@ -399,17 +399,13 @@ def run_mla(a, wl, rank, local_rank, world):
     # ---- end to end through the public API from pinned host buffers
     e2e = None
     if not a.no_e2e:
-        h_h = st.h_new.cpu().pin_memory()
-        q_h = st.q.cpu().pin_memory()
-        p_h = st.pos_new.cpu().pin_memory()
-        s_h = st.seq_lens.cpu().pin_memory()
+        # the step's inputs (new hidden states, queries, positions, lengths)
+        # sit in one pinned staging buffer and go over in one copy
+        in_h = st.step_inputs.cpu().pin_memory()
         out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
 
         def e2e_step():
-            st.h_new.copy_(h_h, non_blocking=True)
-            st.q.copy_(q_h, non_blocking=True)
-            st.pos_new.copy_(p_h, non_blocking=True)
-            st.seq_lens.copy_(s_h, non_blocking=True)
+            st.step_inputs.copy_(in_h, non_blocking=True)
             st.step()
             out_h.copy_(st.out, non_blocking=True)
 
@@ -433,10 +429,11 @@ def run_mla(a, wl, rank, local_rank, world):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": wl.B * wl.T * a.steps * world / (e_ms * 1e-3), "unit": "tokens/s",
-               "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (h_h, q_h, p_h, s_h)),
+               "h2d_bytes_per_step": in_h.numel() * in_h.element_size(),
                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
-               "note": "every step copies its inputs from pinned host memory and its output "
-                       "back inside the timed region (one CUDA graph per step)"}
+               "note": "every step copies its inputs (one packed pinned buffer: new hidden "
+                       "states, queries, positions, lengths) from host memory and its output back "
+                       "inside the timed region (one CUDA graph per step)"}
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

@@ -33,13 +33,28 @@ class DeviceState:
             self.cache = torch.empty((rows, d.row_width), dtype=dt, device=self.dev)
         else:
             self.cache = torch.full((rows, d.row_width), sentinel, dtype=dt, device=self.dev)
-        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=self.dev)
-        self.q = wl.q(device=self.dev).contiguous()
         T = wl.T
-        self.h_new = torch.cat([wl.h_rows(b, L, L + T, device=self.dev)
-                                for b, L in enumerate(wl.lens)]).contiguous()
-        self.pos_new = torch.tensor([L + t for L in wl.lens for t in range(T)],
-                                    dtype=torch.int32, device=self.dev)
+        seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=self.dev)
+        q = wl.q(device=self.dev).contiguous()
+        h_new = torch.cat([wl.h_rows(b, L, L + T, device=self.dev)
+                           for b, L in enumerate(wl.lens)]).contiguous()
+        pos_new = torch.tensor([L + t for L in wl.lens for t in range(T)],
+                               dtype=torch.int32, device=self.dev)
+        # The step's inputs live in one buffer (256-byte aligned parts), so
+        # that a caller can bring a step's inputs over in one copy.
+        parts = [h_new, q, pos_new, seq_lens]
+        offs, off = [], 0
+        for x in parts:
+            offs.append(off)
+            off = (off + x.numel() * x.element_size() + 255) // 256 * 256
+        self.step_inputs = torch.empty(off, dtype=torch.uint8, device=self.dev)
+        views = []
+        for x, o in zip(parts, offs):
+            nb = x.numel() * x.element_size()
+            v = self.step_inputs[o:o + nb].view(x.dtype).view(x.shape)
+            v.copy_(x)
+            views.append(v)
+        self.h_new, self.q, self.pos_new, self.seq_lens = views
         self.out = torch.empty((wl.B, T, d.d_model), dtype=dt, device=self.dev)
         self.ws_bytes = self.mla.workspace_size(wl.B, T, self.bt.shape[1])
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
