@@ -115,6 +115,8 @@ def work_model(wl):
         "out_proj": (D * H * dv * es + M * H * dv * es + M * D * es, 2.0 * M * D * H * dv),
         "plan": (wl.B * 4, 0.0),
     }
+    # one launch runs the append and the absorbed query together
+    k["append_absorb"] = tuple(a + b for a, b in zip(k["compress_append"], k["absorb_q"]))
     tot_bytes = (R * D + H * dn * dc + H * dv * dc + D * H * dv) * es \
         + cache_rows * R * es + M * (D + H * (dn + dr) + D) * es
     tot_flops = sum(k[n][1] for n in ("compress_append", "absorb_q", "attend", "value_proj",
@@ -454,8 +456,8 @@ def run_mla(a, wl, rank, local_rank, world):
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
                    f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
                    "step's event bracket)",
-                   "graph": "each step is one CUDA-graph replay of mla_compress_append + "
-                            "mla_decode",
+                   "graph": "each step is one CUDA-graph replay of mla_append_decode "
+                            "(append the new rows, then decode them)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cache_gbs": cache_bytes / t_step / 1e9,
                    "step_algorithmic_gb": tot_bytes / 1e9,

@@ -146,6 +146,18 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache,
                       const int32_t* seq_lens, int batch, int T, void* out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step: mla_compress_append of the batch*T new tokens followed by
+ * mla_decode of the same tokens, with the arguments, layouts, ownership and
+ * error behaviour of those two calls (normally positions[b*T+t] =
+ * seq_lens[b] - T + t).  Results are those of the two calls bit for bit;
+ * the library may overlap the append with the absorbed-query step, which
+ * does not read the cache. */
+mla_status mla_append_decode(mla_ctx* ctx, const void* h, const int32_t* positions,
+                             const void* q, void* cache, int num_pages,
+                             const int32_t* block_table, int max_pages,
+                             const int32_t* seq_lens, int batch, int T, void* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Decode without a workspace argument, for callers that cannot allocate
  * device memory when they decode (a fixed memory budget reserved up front,
  * an allocator that is not reachable from the issuing thread, a plugin that

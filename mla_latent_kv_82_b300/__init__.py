@@ -29,7 +29,7 @@ EXPORTED = (
     "mla_create", "mla_destroy", "mla_compress_append", "mla_decode_workspace_size",
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
-    "mla_decode_static_workspace",
+    "mla_decode_static_workspace", "mla_append_decode",
 )
 
 
@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
         "mla_status_string": ([i32], ctypes.c_char_p),
         "mla_profile_enable": ([vp, i32], i32),
         "mla_decode_static_workspace": ([vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp], i32),
+        "mla_append_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp],
+                              i32),
         "mla_profile_read": ([vp, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_char_p), i32], i32),
     }
@@ -126,6 +128,12 @@ def mla_decode(ctx, q, cache, num_pages, block_table, max_pages, seq_lens, batch
                workspace, workspace_bytes, stream) -> int:
     return _lib.mla_decode(ctx, q, cache, num_pages, block_table, max_pages, seq_lens, batch, T,
                            out, workspace, workspace_bytes, stream)
+
+
+def mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_pages, seq_lens,
+                      batch, T, out, workspace, workspace_bytes, stream) -> int:
+    return _lib.mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_pages,
+                                  seq_lens, batch, T, out, workspace, workspace_bytes, stream)
 
 
 def mla_decode_static_workspace(ctx, q, cache, num_pages, block_table, max_pages, seq_lens,
@@ -217,6 +225,18 @@ class MLA:
                         self._stream(stream))
         if st != MLA_OK:
             raise MLAError(st, "mla_decode")
+
+    def append_decode(self, h, positions, q, cache, block_table, seq_lens, out, workspace,
+                      stream=None):
+        batch, T = q.shape[0], q.shape[1]
+        st = mla_append_decode(self.ctx, h.data_ptr(), positions.data_ptr(), q.data_ptr(),
+                               cache.data_ptr(), cache.shape[0] // self.dims.page_size,
+                               block_table.data_ptr(), block_table.shape[-1],
+                               seq_lens.data_ptr(), batch, T, out.data_ptr(),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               self._stream(stream))
+        if st != MLA_OK:
+            raise MLAError(st, "mla_append_decode")
 
     def check_status(self, stream=None) -> int:
         return mla_check_status(self.ctx, self._stream(stream))

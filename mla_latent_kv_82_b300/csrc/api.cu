@@ -236,6 +236,48 @@ mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache, int num_pa
   return launch_status();
 }
 
+mla_status mla_append_decode(mla_ctx* ctx, const void* h, const int32_t* positions,
+                             const void* q, void* cache, int num_pages,
+                             const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                             int batch, int T, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!ctx || !h || !positions || !q || !cache || !block_table || !seq_lens || !out ||
+      !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || T < 1 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (T > 8 || (long long)batch * max_pages > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+  const size_t a = ctx->cfg.dtype == MLA_BF16 ? 16 : 4;
+  if (!aligned(h, a) || !aligned(q, a) || !aligned(cache, a) || !aligned(out, a) ||
+      !aligned(workspace, 256) || !aligned(positions, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  const mla::WsLayout L = mla::workspace_layout(ctx, batch, T, max_pages);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  bool launched = true;
+  if (ctx->cfg.dtype == MLA_BF16) {
+    launched = mla::bf16_append_decode(
+        ctx, static_cast<const __nv_bfloat16*>(h), positions, static_cast<const __nv_bfloat16*>(q),
+        static_cast<__nv_bfloat16*>(cache), num_pages, block_table, max_pages, seq_lens, batch, T,
+        static_cast<__nv_bfloat16*>(out), ws, L, st);
+  } else {
+    mla::f32_compress_append(ctx, static_cast<const float*>(h), batch, T, positions, block_table,
+                             max_pages, static_cast<float*>(cache), num_pages, st);
+    mla::prof_mark(ctx, st, "plan");
+    mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
+    ctx->launches += 1;
+    mla::f32_decode(ctx, static_cast<const float*>(q), static_cast<const float*>(cache),
+                    num_pages, block_table, max_pages, batch, T, static_cast<float*>(out), ws,
+                    L, st);
+  }
+  mla::prof_mark(ctx, st, nullptr);
+  if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  return launch_status();
+}
+
 mla_status mla_check_status(mla_ctx* ctx, void* stream) {
   if (!ctx) return MLA_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);

@@ -243,11 +243,12 @@ void bf16_teardown(mla_ctx* ctx) {
   ctx->counters = nullptr;
 }
 
-bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
-                          const int32_t* pos, const int32_t* bt, int max_pages,
-                          __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
+// GEMM plan of the compress + RoPE + paged append step.
+static bool append_plan(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T, const int32_t* pos,
+                        const int32_t* bt, int max_pages, __nv_bfloat16* cache, int num_pages,
+                        WgPlan& p) {
   const int M = B * T, D = ctx->cfg.d_model;
-  WgPlan p{};
+  p = WgPlan{};
   const GemmShape g = gemm_shape(ctx, M, 5, D / 64, 8, kAppendPartialBytes);
   p.nt = g.nt;
   p.n_tiles = g.n_tiles;
@@ -275,6 +276,14 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
   a.T = T;
   a.append_rope_tile = 4;
   a.partials = ctx->append_partials;
+  return true;
+}
+
+bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
+                          const int32_t* pos, const int32_t* bt, int max_pages,
+                          __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
+  WgPlan p;
+  if (!append_plan(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, p)) return false;
   prof_mark(ctx, st, "compress_append");
   ctx->launches += 1;
   return check(wgemm_launch(p, WG_APPEND, false, st, true));
@@ -283,7 +292,7 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
 bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
                  int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
                  int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
-                 cudaStream_t st) {
+                 cudaStream_t st, const WgPlan* append) {
   const int M = B * T, D = ctx->cfg.d_model;
   const Bf16Plans bp = decode_plans(ctx, M);
   if (bp.abs.n_tiles > 65535 || bp.uv.n_tiles > 65535 || bp.o.n_tiles > 65535) return false;
@@ -322,9 +331,21 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
                       reinterpret_cast<int*>(ws + L.first_split),
                       reinterpret_cast<int*>(ws + L.slot_base), reinterpret_cast<int*>(ws + L.meta),
                       ctx->status};
-    prof_mark(ctx, st, "absorb_q");
-    ctx->launches += 1;
-    if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
+    if (append && (append->nt == 16 || append->nt == 32)) {
+      // the append and the absorbed query share no data: one launch
+      prof_mark(ctx, st, "append_absorb");
+      ctx->launches += 1;
+      if (!check(wgemm_launch_dual(*append, p, st, true))) return false;
+    } else {
+      if (append) {
+        prof_mark(ctx, st, "compress_append");
+        ctx->launches += 1;
+        if (!check(wgemm_launch(*append, WG_APPEND, false, st, true))) return false;
+      }
+      prof_mark(ctx, st, "absorb_q");
+      ctx->launches += 1;
+      if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
+    }
   }
   // ---- split-KV attention over the latent cache
   const bool paired = T % 2 == 0;   // tokens 2j, 2j+1 share every cache tile
@@ -413,6 +434,15 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     if (!check(wgemm_launch(p, WG_ROWMAJOR, false, st, true))) return false;
   }
   return true;
+}
+
+bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos,
+                        const __nv_bfloat16* q, __nv_bfloat16* cache, int num_pages,
+                        const int32_t* bt, int max_pages, const int32_t* seq_lens, int B, int T,
+                        __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st) {
+  WgPlan p;
+  if (!append_plan(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, p)) return false;
+  return bf16_decode(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st, &p);
 }
 
 }  // namespace mla

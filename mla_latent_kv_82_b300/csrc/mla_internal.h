@@ -73,10 +73,18 @@ void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,
 bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           const int32_t* pos, const int32_t* bt, int max_pages,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st);
+struct WgPlan;
+// `append` (optional): the append step's GEMM plan, run in the same launch
+// as the absorbed query (the two share no data).
 bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
                  int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
                  int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
-                 cudaStream_t st);
+                 cudaStream_t st, const WgPlan* append = nullptr);
+// Append the B*T new rows, then decode them (mla_append_decode).
+bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos,
+                        const __nv_bfloat16* q, __nv_bfloat16* cache, int num_pages,
+                        const int32_t* bt, int max_pages, const int32_t* seq_lens, int B, int T,
+                        __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
 
 // bf16 path helpers
 bool bf16_setup(mla_ctx* ctx);                 // weight maps + scratch, at create

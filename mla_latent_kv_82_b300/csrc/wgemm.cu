@@ -41,10 +41,11 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// One CTA's work: weight tile mt, token tile nt (of ntile), K split z.
 template <int NT, int EPI, bool A_MN>
-__global__ void __launch_bounds__(kThreads, WgCfg<NT>::kMinBlocks)
-wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-             const __grid_constant__ CUtensorMap tmB, const WgArgs a) {
+__device__ __forceinline__ void wgemm_body(const CUtensorMap& tmA, const CUtensorMap& tmA2,
+                                           const CUtensorMap& tmB, const WgArgs& a, const int mt,
+                                           const int nt, const int z, const int ntile) {
   using C = WgCfg<NT>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -58,7 +59,6 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   int* scan_tmp = reinterpret_cast<int*>(smem + S * C::kStage + 256);     // 33 ints
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y, z = blockIdx.z;
   const int head = mt / a.tiles_per_head, tile = mt % a.tiles_per_head;
   const int kc0 = z * a.k_chunks / a.splits, kc1 = (z + 1) * a.k_chunks / a.splits;
   const int nk = kc1 - kc0;
@@ -169,7 +169,6 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     if (etid == 0) flags[2] = flags[0];
     tc::named_sync(1, 128);
     const bool ok = flags[2] == 0;
-    const int ntile = gridDim.y;
     float* part = nullptr;
     bool final_cta = true;
     if (ok && a.splits > 1) {
@@ -321,6 +320,81 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 }
 
 template <int NT, int EPI, bool A_MN>
+__global__ void __launch_bounds__(kThreads, WgCfg<NT>::kMinBlocks)
+wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+             const __grid_constant__ CUtensorMap tmB, const WgArgs a) {
+  wgemm_body<NT, EPI, A_MN>(tmA, tmA2, tmB, a, blockIdx.x, blockIdx.y, blockIdx.z, gridDim.y);
+}
+
+// The compress/append GEMM (first m1 * n1 * s1 CTAs, token tile NT1) and the
+// absorbed-query GEMM (token tile NT2) in one launch: they share no data, so
+// one waits for nothing of the other.
+template <int NT1, int NT2>
+struct DualCfg {
+  static constexpr int kMinBlocks =
+      WgCfg<NT1>::kMinBlocks < WgCfg<NT2>::kMinBlocks ? WgCfg<NT1>::kMinBlocks : WgCfg<NT2>::kMinBlocks;
+  static constexpr uint32_t kSmem =
+      WgCfg<NT1>::kSmem > WgCfg<NT2>::kSmem ? WgCfg<NT1>::kSmem : WgCfg<NT2>::kSmem;
+};
+
+template <int NT1, int NT2>
+__global__ void __launch_bounds__(kThreads, (DualCfg<NT1, NT2>::kMinBlocks))
+wgemm_dual_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA21,
+                  const __grid_constant__ CUtensorMap tmB1, const WgArgs a1,
+                  const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA22,
+                  const __grid_constant__ CUtensorMap tmB2, const WgArgs a2, const int m1,
+                  const int n1, const int s1, const int m2, const int n2) {
+  const int c1 = m1 * n1 * s1;
+  const int bid = blockIdx.x;
+  if (bid < c1) {
+    wgemm_body<NT1, WG_APPEND, false>(tmA1, tmA21, tmB1, a1, bid % m1, (bid / m1) % n1,
+                                      bid / (m1 * n1), n1);
+  } else {
+    const int b = bid - c1;
+    wgemm_body<NT2, WG_QIMG, true>(tmA2, tmA22, tmB2, a2, b % m2, (b / m2) % n2, b / (m2 * n2), n2);
+  }
+}
+
+template <int NT1, int NT2>
+cudaError_t launch_dual_nt(const WgPlan& p1, const WgPlan& p2, cudaStream_t st, bool pdl) {
+  using C = DualCfg<NT1, NT2>;
+  auto kern = wgemm_dual_kernel<NT1, NT2>;
+  static bool attr_set = false;   // per instantiation, set once per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int c1 = p1.m_tiles * p1.n_tiles * p1.args.splits;
+  const int c2 = p2.m_tiles * p2.n_tiles * p2.args.splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c1 + c2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p1.tmA, p1.tmA2, p1.tmB, p1.args, p2.tmA, p2.tmA2, p2.tmB,
+                            p2.args, p1.m_tiles, p1.n_tiles, p1.args.splits, p2.m_tiles,
+                            p2.n_tiles);
+}
+
+template <int NT1>
+cudaError_t launch_dual_nt1(const WgPlan& p1, const WgPlan& p2, cudaStream_t st, bool pdl) {
+  switch (p2.nt) {
+    case 16: return launch_dual_nt<NT1, 16>(p1, p2, st, pdl);
+    case 32: return launch_dual_nt<NT1, 32>(p1, p2, st, pdl);
+    case 64: return launch_dual_nt<NT1, 64>(p1, p2, st, pdl);
+    case 128: return launch_dual_nt<NT1, 128>(p1, p2, st, pdl);
+    default: return launch_dual_nt<NT1, 256>(p1, p2, st, pdl);
+  }
+}
+
+template <int NT, int EPI, bool A_MN>
 cudaError_t launch_nt(const WgPlan& p, cudaStream_t st, bool pdl) {
   using C = WgCfg<NT>;
   auto kern = wgemm_kernel<NT, EPI, A_MN>;
@@ -366,6 +440,12 @@ int wgemm_token_tile(int n_tokens) {
 }
 
 int wgemm_ctas_per_sm(int nt) { return nt <= 64 ? 2 : 1; }
+
+cudaError_t wgemm_launch_dual(const WgPlan& append, const WgPlan& qimg, cudaStream_t st, bool pdl) {
+  if (append.nt == 16) return launch_dual_nt1<16>(append, qimg, st, pdl);
+  if (append.nt == 32) return launch_dual_nt1<32>(append, qimg, st, pdl);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t wgemm_launch(const WgPlan& p, int epi, bool a_mn_major, cudaStream_t st, bool pdl) {
   if (a_mn_major) return launch_epi<WG_QIMG, true>(p, st, pdl);

@@ -53,5 +53,8 @@ struct WgPlan {
 int wgemm_token_tile(int n_tokens);
 int wgemm_ctas_per_sm(int nt);
 cudaError_t wgemm_launch(const WgPlan& p, int epi, bool a_mn_major, cudaStream_t st, bool pdl);
+// A WG_APPEND plan (token tile 16 or 32) and a WG_QIMG plan (MN-major) in one
+// launch; cudaErrorInvalidValue for another append token tile.
+cudaError_t wgemm_launch_dual(const WgPlan& append, const WgPlan& qimg, cudaStream_t st, bool pdl);
 
 }  // namespace mla

@@ -80,6 +80,13 @@ class DeviceState:
                         stream=stream)
 
     def step(self, stream=None):
+        """Append the T new tokens of every sequence, then decode them (one
+        mla_append_decode call)."""
+        self.mla.append_decode(self.h_new, self.pos_new, self.q, self.cache, self.bt,
+                               self.seq_lens, self.out, self.ws, stream=stream)
+
+    def step_separate(self, stream=None):
+        """The same step as two calls: mla_compress_append, then mla_decode."""
         self.append_new(stream)
         self.decode(stream)
 

@@ -140,6 +140,28 @@ def test_bad_page_id_is_reported_not_written():
     assert st.mla.check_status() == 0      # the status word was cleared
 
 
+@pytest.mark.parametrize("make", [
+    lambda: tiny_f32([5, 40, 64], 1),
+    lambda: small_bf16([0, 63, 200, 1000], 1),
+    lambda: small_bf16([62, 127, 500], 2),
+    lambda: W.config("b1-l4096"),
+])
+def test_append_decode_equals_two_calls(make):
+    """mla_append_decode (one call; the append may run in the absorbed-query
+    launch) gives the cache rows and outputs of mla_compress_append followed
+    by mla_decode, bit for bit."""
+    from mla_latent_kv_82_b300.workload import DeviceState
+    wl = make()
+    one = DeviceState(wl, sentinel=0.0)
+    two = DeviceState(wl, sentinel=0.0)
+    one.step()
+    two.step_separate()
+    torch.cuda.synchronize()
+    assert one.mla.check_status() == 0 and two.mla.check_status() == 0
+    assert torch.equal(one.cache.view(torch.uint8), two.cache.view(torch.uint8))
+    assert torch.equal(one.out.view(torch.uint8), two.out.view(torch.uint8))
+
+
 def test_bad_length_is_reported():
     wl = small_bf16([10], 1)
     from mla_latent_kv_82_b300.workload import DeviceState

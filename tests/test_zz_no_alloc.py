@@ -33,7 +33,7 @@ def test_static_workspace_matches_workspace_decode(T, lens):
     from mla_latent_kv_82_b300.workload import DeviceState
 
     st = DeviceState(small_bf16(lens, T))
-    st.step()                                  # append + regular mla_decode
+    st.step()                                  # append + decode (workspace argument)
     torch.cuda.synchronize()
     assert st.mla.check_status() == 0
     ref = to_np(st.out)
