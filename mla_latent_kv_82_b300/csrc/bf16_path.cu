@@ -7,6 +7,7 @@
 // Every launch after the first of a call uses programmatic dependent launch.
 #include <algorithm>
 
+#include "gemv.h"
 #include "layouts.cuh"
 #include "tmap.h"
 #include "wgemm.h"
@@ -408,7 +409,14 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     if (!check(wgemm_launch(p, WG_ROWMAJOR, false, st, true))) return false;
   }
   // ---- output projection: u = W_O o
-  {
+  GemvArgs go{static_cast<const __nv_bfloat16*>(ctx->w.w_o), D, kHeads * kDv, M, o,
+              (long long)kHeads * kDv, D, 0, out, (long long)D};
+  if (gemv_supported(go, ctx->num_sms)) {
+    // one or two tokens: a matrix-vector product, bound by streaming W_O
+    prof_mark(ctx, st, "out_proj");
+    ctx->launches += 1;
+    if (!check(gemv_launch(go, ctx->num_sms, st, true))) return false;
+  } else {
     WgPlan p{};
     p.nt = bp.o.nt;
     p.n_tiles = bp.o.n_tiles;

@@ -58,6 +58,9 @@ def _compare_all(st, form="explicit", seqs=None):
 @pytest.mark.parametrize("T,lens", [
     (1, [0, 62, 63, 64, 200, 1000]),
     (2, [0, 62, 63, 127, 500]),
+    (1, [300]),          # one token: the projections run as GEMVs
+    (2, [200]),          # two tokens: GEMVs, and the paired attention
+    (1, [70, 1]),        # two tokens from two sequences
 ])
 def test_small_bf16_explicit(T, lens):
     st = _run(small_bf16(lens, T))
