@@ -38,6 +38,7 @@
 // bounded; a failure sets both CTAs' abort flags.
 #include "attend_common.cuh"
 #include "tmap.h"
+#include "launch_util.h"
 
 namespace mla {
 namespace {
@@ -508,13 +509,8 @@ bool tc_attend_pair(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attend_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPSmem) != cudaSuccess)
-      return false;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (smem_attr_once(attr_done, attend_pair_kernel, (int)kPSmem) != cudaSuccess) return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(T, L.G, 2);
   cfg.blockDim = dim3(256);

@@ -31,6 +31,7 @@
 // own loads and frees TMEM.
 #include "attend_common.cuh"
 #include "tmap.h"
+#include "launch_util.h"
 
 namespace mla {
 namespace {
@@ -367,13 +368,8 @@ bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
   a.max_pages = max_pages;
   a.num_pages = num_pages;
   a.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem) != cudaSuccess)
-      return false;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (smem_attr_once(attr_done, attend_tc_kernel, (int)kSmem) != cudaSuccess) return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.G, T, 2);
   cfg.blockDim = dim3(224);

@@ -20,6 +20,7 @@
 
 #include "device_util.cuh"
 #include "gemv.h"
+#include "launch_util.h"
 
 namespace mla {
 namespace {
@@ -141,13 +142,8 @@ gemv_kernel(const __nv_bfloat16* __restrict__ W, int R, int K, const __nv_bfloat
 template <int M>
 cudaError_t launch_m(const GemvArgs& g, int ctas, cudaStream_t st, bool pdl) {
   auto kern = gemv_kernel<M>;
-  static bool attr_set = false;   // per instantiation, set once per process
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};   // per instantiation
+  if (const cudaError_t e = smem_attr_once(attr_done, kern, (int)kSmem); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);

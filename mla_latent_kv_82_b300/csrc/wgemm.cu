@@ -19,6 +19,7 @@
 #include "layouts.cuh"
 #include "tc_util.cuh"
 #include "wgemm.h"
+#include "launch_util.h"
 
 namespace mla {
 namespace {
@@ -359,13 +360,9 @@ template <int NT1, int NT2>
 cudaError_t launch_dual_nt(const WgPlan& p1, const WgPlan& p2, cudaStream_t st, bool pdl) {
   using C = DualCfg<NT1, NT2>;
   auto kern = wgemm_dual_kernel<NT1, NT2>;
-  static bool attr_set = false;   // per instantiation, set once per process
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};   // per instantiation
+  if (const cudaError_t e = smem_attr_once(attr_done, kern, (int)C::kSmem); e != cudaSuccess)
+    return e;
   const int c1 = p1.m_tiles * p1.n_tiles * p1.args.splits;
   const int c2 = p2.m_tiles * p2.n_tiles * p2.args.splits;
   cudaLaunchConfig_t cfg = {};
@@ -398,13 +395,9 @@ template <int NT, int EPI, bool A_MN>
 cudaError_t launch_nt(const WgPlan& p, cudaStream_t st, bool pdl) {
   using C = WgCfg<NT>;
   auto kern = wgemm_kernel<NT, EPI, A_MN>;
-  static bool attr_set = false;   // per instantiation, set once per process
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};   // per instantiation
+  if (const cudaError_t e = smem_attr_once(attr_done, kern, (int)C::kSmem); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.m_tiles, p.n_tiles, p.args.splits);
   cfg.blockDim = dim3(kThreads);
