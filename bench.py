@@ -245,6 +245,22 @@ def time_oracle(wl, st, steps=None, seconds=None):
     return per_step_tokens * n / el, el, n, sample
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest of every rank's x (the slowest rank's time); x at N = 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Units all ranks processed per second over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (total_ms * 1e-3)
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -341,11 +357,7 @@ def run_mla(a, wl, rank, local_rank, world):
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    step_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
-    if world > 1:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs), dev)
     status = st.mla.check_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -353,8 +365,7 @@ def run_mla(a, wl, rank, local_rank, world):
     clocks.stop()
     launches = launches_per_step * a.steps
 
-    tokens = wl.B * wl.T * a.steps * world
-    value = tokens / (step_ms * 1e-3)
+    value = whole_job_rate(wl.B * wl.T, a.steps, world, step_ms)
     ms_per_step = step_ms / a.steps
 
     # ---- per-kernel durations: the same steps with an event at every kernel
@@ -425,12 +436,8 @@ def run_mla(a, wl, rank, local_rank, world):
             g_e2e.replay()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = sum(e0.elapsed_time(e1) for e0, e1 in ev)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": wl.B * wl.T * a.steps * world / (e_ms * 1e-3), "unit": "tokens/s",
+        e_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev), dev)
+        e2e = {"value": whole_job_rate(wl.B * wl.T, a.steps, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": in_h.numel() * in_h.element_size(),
                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
                "note": "every step copies its inputs (one packed pinned buffer: new hidden "

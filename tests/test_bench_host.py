@@ -1,0 +1,89 @@
+"""bench.py host logic on CPU: the multi-rank aggregation (gloo ranks stand
+in for GPU ranks: every rank runs an independent replica, the job's time is
+the slowest rank's and its throughput counts every rank's tokens) and the
+reference arm's JSON line, alone and under torchrun with two ranks."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, times, out):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(times[rank], "cpu")
+        rate = bench.whole_job_rate(4, 10, world, ms)
+        out.put((rank, ms, rate))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_sets_the_time_and_every_rank_counts():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    times = [12.5, 20.0]
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, times, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, rate in res:
+        assert ms == 20.0                                   # max over ranks, on every rank
+        assert rate == pytest.approx(4 * 10 * 2 / 20e-3)    # all ranks' tokens / slowest time
+
+
+def test_single_rank_is_unchanged():
+    assert bench.max_over_ranks(7.0) == 7.0
+    assert bench.whole_job_rate(1, 1000, 1, 80.0) == pytest.approx(12500.0)
+
+
+def _json_lines(out: str):
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_prints_one_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny-fp32", "--steps", "3", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    j = lines[0]
+    assert j["impl"] == "reference" and j["unit"] == "tokens/s" and j["value"] > 0
+    assert j["metric"] == bench.METRIC and j["higher_is_better"] is True
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"] == {"value": j["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_under_torchrun_prints_on_rank_zero_only():
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(_free_port()),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--config", "tiny-fp32", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
