@@ -61,6 +61,8 @@ def _compare_all(st, form="explicit", seqs=None):
     (1, [300]),          # one token: the projections run as GEMVs
     (2, [200]),          # two tokens: GEMVs, and the paired attention
     (1, [70, 1]),        # two tokens from two sequences
+    (3, [2, 64, 190]),   # odd T > 1: single-CTA kernel, three tokens per split
+    (4, [3, 130, 260]),  # T = 4: two CTA pairs per split
 ])
 def test_small_bf16_explicit(T, lens):
     st = _run(small_bf16(lens, T))
@@ -73,7 +75,8 @@ def test_small_bf16_latent_output():
 
 
 @pytest.mark.parametrize("T,lens,page", [
-    (1, [63], 64), (1, [0, 15, 16, 17, 100], 16), (2, [0, 14, 15, 33], 16), (1, [40, 3], 1)])
+    (1, [63], 64), (1, [0, 15, 16, 17, 100], 16), (2, [0, 14, 15, 33], 16), (1, [40, 3], 1),
+    (3, [0, 20, 47], 16)])
 def test_tiny_f32(T, lens, page):
     st = _run(tiny_f32(lens, T, page))
     _compare_all(st, "explicit")
