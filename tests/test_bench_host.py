@@ -87,3 +87,26 @@ def test_reference_arm_under_torchrun_prints_on_rank_zero_only():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_work_model_matches_closed_forms():
+    """The roofline numerators at DeepSeek-V2 widths (d = 5120, 128 heads of
+    128, d_c = 512, d_R = 64): weight bytes read once, one 576-wide bf16 row
+    per cached token, 2 FLOP per multiply-add."""
+    from synth import workloads as W
+    k, tot_bytes, tot_flops, cache_bytes = bench.work_model(W.config("b1-l4096"))
+    assert k["out_proj"][0] == 5120 * 16384 * 2 + 16384 * 2 + 5120 * 2   # W_O + o + u
+    assert k["out_proj"][1] == 2 * 5120 * 16384
+    assert k["compress_append"][0] == 576 * 5120 * 2 + 5120 * 2 + 576 * 2
+    assert k["absorb_q"][1] == 2 * 128 * 128 * 512
+    assert cache_bytes == 4096 * 576 * 2
+    # attention: every query token sees its 4096 rows; S over 576 features
+    # and O over 512 latent columns for each of 128 heads
+    assert k["attend"][1] == 2 * 4096 * 128 * (576 + 512)
+    assert k["append_absorb"] == tuple(a + b for a, b in zip(k["compress_append"], k["absorb_q"]))
+    weights = (576 * 5120 + 128 * 128 * 512 + 128 * 128 * 512 + 5120 * 16384) * 2
+    assert tot_bytes == weights + cache_bytes + (5120 + 128 * 192 + 5120) * 2
+    # causal T = 2: the first new token does not see the second
+    k2, _, _, _ = bench.work_model(W.config("b128-l16k-t2"))
+    vis = sum(2 * S - 1 for S in W.config("b128-l16k-t2").seq_lens)
+    assert k2["attend"][1] == 2 * vis * 128 * (576 + 512)
