@@ -9,8 +9,12 @@ when the timed region starts; L2 is flushed (a 2x-L2 buffer is written,
 then another is read) before every timed step, outside the step's own
 CUDA-event bracket.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b1-l4096]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b128-l16k-t2]
                   [--impl mla|reference]
+
+The default workload is the full layer step at DeepSeek-V2 widths (batch
+128, 16384 cached tokens, two query tokens): the largest single-GPU
+workload, on which the throughput metric is quoted.
 
 --impl reference times the fp64 CPU oracle (the reference of this build)
 on the same workload, a bounded sample per step.  Under torchrun (N > 1)
@@ -41,7 +45,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="b1-l4096",
+    ap.add_argument("--config", default="b128-l16k-t2",
                     choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2"])
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -471,6 +475,10 @@ def run_mla(a, wl, rank, local_rank, world):
                    "step_algorithmic_gflop": tot_flops / 1e9,
                    "step_roofline_frac": step_roof / t_step,
                    "kernel_ms": {k: round(v, 5) for k, v in avg.items()},
+                   "kernel_ms_note": "per-kernel times come from a second pass with a CUDA "
+                                     "event at every kernel boundary (events keep kernels from "
+                                     "overlapping, so they sum to more than ms_per_step, which is "
+                                     "timed without them); kernel_share is their ratio",
                    "kernel_share": {k: round(v / sum(share.values()), 4) for k, v in share.items()}},
         "roofline": roof,
         "cpu_baseline": cpu,

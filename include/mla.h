@@ -170,8 +170,10 @@ mla_status mla_append_decode(mla_ctx* ctx, const void* h, const int32_t* positio
  * The call itself allocates nothing.  Shapes whose
  * mla_decode_workspace_size exceeds 32 MiB return MLA_ERR_WORKSPACE before
  * anything is enqueued.  The first call on a device looks up the array's
- * device address (once per device); make that first call before any stream
- * capture.  All calls share the one array, so calls that overlap on the GPU
+ * device address (once per device) and keeps it for the life of the
+ * process; make that first call before any stream capture.  A
+ * cudaDeviceReset of that device invalidates the kept address: do not call
+ * this entry point on a device after resetting it.  All calls share the one array, so calls that overlap on the GPU
  * (other streams, threads or contexts) race and give wrong results; nothing
  * in it needs to be cleared between calls. */
 mla_status mla_decode_static_workspace(mla_ctx* ctx, const void* q,

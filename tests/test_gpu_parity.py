@@ -36,7 +36,7 @@ def _run(wl, sentinel=None, block_table=None):
     return st
 
 
-def _compare_all(st, form="explicit", seqs=None):
+def _compare_all(st, form="explicit", seqs=None, keep_rows=None):
     wl = st.wl
     w64 = ocase.weights_f64(wl, device=DEV)
     q64 = to_np(st.q)
@@ -45,6 +45,8 @@ def _compare_all(st, form="explicit", seqs=None):
     stats = []
     for b in (range(wl.B) if seqs is None else seqs):
         rows, res = oracle_sequence(wl, b, w64, q64, form, DEV)
+        if keep_rows is not None:
+            keep_rows[b] = rows
         check(to_np(pool_rows_of(st, b)), rows, wl.dtype, f"cache rows b={b}")
         stats.append(check(to_np(st.out[b]), res["u"], wl.dtype, f"u b={b}"))
         m = slice(b * wl.T, (b + 1) * wl.T)
@@ -197,15 +199,52 @@ def test_b1_l4096_full():
     _compare_all(st, "explicit")
 
 
-@pytest.mark.parametrize("name,seqs", [
-    ("b64-paged", [0, 7, 21, 33, 40, 63]),
-    ("b128-l16k-t2", [0, 127]),
-    ("b4-l128k", [3]),
-])
-def test_full_configs_sampled(name, seqs):
+FULL_SAMPLES = {
+    # seeded samples of sequences (all four of b4-l128k)
+    "b64-paged": [0, 7, 21, 33, 40, 52, 58, 63],
+    "b128-l16k-t2": [0, 17, 38, 64, 77, 99, 111, 127],
+    "b4-l128k": [0, 1, 2, 3],
+}
+
+
+def _explicit_heads(wl, rows, q_b, w64, heads):
+    """The explicit (non-absorbed) oracle on single heads: K^C and V of each
+    head materialised from the rows, its o returned per head."""
+    import dataclasses
+    from oracle import mla as omla
+    d = wl.dims
+    one = dataclasses.replace(d, n_heads=1)
+    out = {}
+    for h in heads:
+        w = {"w_uk": w64["w_uk"][h * d.d_nope:(h + 1) * d.d_nope],
+             "w_uv": w64["w_uv"][h * d.d_v:(h + 1) * d.d_v],
+             "w_o": w64["w_o"][:, h * d.d_v:(h + 1) * d.d_v]}
+        out[h] = omla.decode_explicit(one, rows, q_b[:, h:h + 1], w, wl.T)["o"][:, 0]
+    return out
+
+
+@pytest.mark.parametrize("name", list(FULL_SAMPLES))
+def test_full_configs_sampled(name):
+    """Full-size workloads in the launch configuration the benchmark times:
+    sampled sequences against the absorbed oracle (u, o, o_lat, cache rows)
+    and, on two heads of each, the value output o against the explicit form."""
     wl = W.config(name)
+    seqs = FULL_SAMPLES[name]
     st = _run(wl)
-    stats = _compare_all(st, "absorbed", seqs=seqs)
+    rows_of = {}
+    stats = _compare_all(st, "absorbed", seqs=seqs, keep_rows=rows_of)
     assert len(stats) == len(seqs)
+    w64 = ocase.weights_f64(wl, device=DEV)
+    q64 = to_np(st.q)
+    o = st.workspace_view("o")
+    rng = np.random.default_rng(2)
+    d = wl.dims
+    for b in seqs:
+        rows = rows_of[b]
+        heads = [int(x) for x in rng.choice(d.n_heads, 2, replace=False)]
+        ref = _explicit_heads(wl, rows, q64[b], w64, heads)
+        for h in heads:
+            got = to_np(o[b * wl.T:(b + 1) * wl.T, h * d.d_v:(h + 1) * d.d_v])
+            check(got, ref[h], wl.dtype, f"o explicit b={b} head={h}")
     # every sequence produced finite output
     assert torch.isfinite(st.out.float()).all()
