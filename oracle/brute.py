@@ -76,3 +76,16 @@ def decode(dims, h, q, w, T):
             concat_o.extend(o_i)
         u_all.append(_matvec(w["w_o"], concat_o))
     return u_all
+
+
+def query(dims, h_row, w):
+    """Scalar query of one hidden row: [n_h][d_nope + d_R], q^R un-rotated.
+
+    c^Q = W^DQ h, q^C = W^UQ c^Q and q^R = W^QR h, head i taking its rows
+    of each (the decode rotates q^R at the query position).
+    """
+    H, dn, dr = dims.n_heads, dims.d_nope, dims.d_rope
+    c_q = _matvec(w["w_dq"], h_row)
+    q_c = _matvec(w["w_uq"], c_q)
+    q_r = _matvec(w["w_qr"], h_row)
+    return [q_c[i * dn:(i + 1) * dn] + q_r[i * dr:(i + 1) * dr] for i in range(H)]

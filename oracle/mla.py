@@ -106,6 +106,32 @@ def slot_of(block_table: np.ndarray, b: int, pos: int, page_size: int) -> int:
 
 
 # ---------------------------------------------------------------------------
+# Query path ([V2-arch] ch.2 §2, last paragraph: the query gets the same
+# low-rank compression, c^Q; [DS-report] "RoPE 的兼容性处理":
+# q_t = [W^UQ c_t^Q ; W^QR h_t . RoPE(t)])
+# ---------------------------------------------------------------------------
+def query_from_hidden(dims, h: np.ndarray, w_dq: np.ndarray, w_uq: np.ndarray,
+                      w_qr: np.ndarray) -> np.ndarray:
+    """Decode queries [N, n_h, d_nope + d_R] of hidden states ``h`` [N, d].
+
+    c^Q = W^DQ h (reading: the query's down-projection, in the form of
+    c^KV = W^DKV h; its width d_c' is not on the pages and is a parameter);
+    q^C = W^UQ c^Q, head i owning rows i*d_nope..; q^R = W^QR h as the
+    report writes it (input h, not c^Q), head i owning rows i*d_R...  The
+    rotation of q^R is left to the decode, which applies it at the query's
+    position, so the result has the layout of the decode's ``q`` input.
+    Matrices act on column vectors: W^DQ [d_c', d], W^UQ [n_h*d_nope, d_c'],
+    W^QR [n_h*d_R, d].
+    """
+    h = np.asarray(h, dtype=np.float64)
+    H, dn, dr = dims.n_heads, dims.d_nope, dims.d_rope
+    c_q = h @ np.asarray(w_dq, dtype=np.float64).T
+    q_c = (c_q @ np.asarray(w_uq, dtype=np.float64).T).reshape(-1, H, dn)
+    q_r = (h @ np.asarray(w_qr, dtype=np.float64).T).reshape(-1, H, dr)
+    return np.concatenate([q_c, q_r], axis=2)
+
+
+# ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------
 def _softmax(s: np.ndarray) -> np.ndarray:

@@ -334,3 +334,118 @@ def test_planted_unmasked_future(monkeypatch):
         return res
     monkeypatch.setattr(mla, "decode_explicit", bad)
     assert not _pins_pass()
+
+
+# --------------------------------------------------------------------------
+# query path: c^Q = W^DQ h, q^C = W^UQ c^Q, q^R = W^QR h
+# --------------------------------------------------------------------------
+QW = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o", "w_dq", "w_uq", "w_qr")
+
+
+def _qdims(case):
+    return dataclasses.replace(WORKED_DIMS, n_heads=case["n_heads"])
+
+
+def _query_worked(case, decode_fn):
+    dims = _qdims(case)
+    w = {k: np.array(case[k], dtype=np.float64) for k in QW}
+    h = np.array(case["h"])
+    rows = _rows(dims, w, h)
+    q = mla.query_from_hidden(dims, h[-1:], w["w_dq"], w["w_uq"], w["w_qr"])
+    return q, decode_fn(dims, rows, q, w, 1)["u"][0]
+
+
+@pytest.mark.parametrize("form", ["explicit", "absorbed"])
+def test_query_path_worked_examples(form):
+    fn = mla.decode_explicit if form == "explicit" else mla.decode_absorbed
+    for case in _load("query_path_examples.json")["cases"]:
+        q, u = _query_worked(case, fn)
+        np.testing.assert_allclose(q, case["expect_q"], rtol=0, atol=1e-14, err_msg=case["name"])
+        np.testing.assert_allclose(u, case["expect_u"], rtol=0, atol=1e-14, err_msg=case["name"])
+
+
+def test_query_path_worked_examples_brute():
+    for case in _load("query_path_examples.json")["cases"]:
+        dims = _qdims(case)
+        w = {k: case[k] for k in QW}
+        q = brute.query(dims, case["h"][-1], w)
+        np.testing.assert_allclose(q, case["expect_q"][0], rtol=0, atol=1e-14, err_msg=case["name"])
+        u = brute.decode(dims, case["h"], [q], w, 1)[0]
+        np.testing.assert_allclose(u, case["expect_u"], rtol=0, atol=1e-14, err_msg=case["name"])
+
+
+@pytest.mark.parametrize("dims", SMALL_SHAPES)
+@pytest.mark.parametrize("d_cq", [3, 7])
+def test_query_path_brute_force_agrees(dims, d_cq):
+    rng = np.random.default_rng(d_cq)
+    d = dims
+    w = {"w_dq": rng.standard_normal((d_cq, d.d_model)),
+         "w_uq": rng.standard_normal((d.n_heads * d.d_nope, d_cq)),
+         "w_qr": rng.standard_normal((d.n_heads * d.d_rope, d.d_model))}
+    h = rng.standard_normal((3, d.d_model))
+    q = mla.query_from_hidden(d, h, w["w_dq"], w["w_uq"], w["w_qr"])
+    ref = [brute.query(d, list(r), {k: v.tolist() for k, v in w.items()}) for r in h]
+    assert _rel(q, np.array(ref)) < 1e-12
+
+
+def _query_pins_pass():
+    try:
+        test_query_path_worked_examples("explicit")
+        test_query_path_brute_force_agrees(SMALL_SHAPES[1], 3)
+    except AssertionError:
+        return False
+    return True
+
+
+def test_query_pins_pass_unplanted():
+    assert _query_pins_pass()
+
+
+def test_planted_query_rope_from_latent(monkeypatch):
+    """q^R taken from c^Q instead of h (a plausible misreading)."""
+    def bad(dims, h, w_dq, w_uq, w_qr):
+        H, dn, dr = dims.n_heads, dims.d_nope, dims.d_rope
+        c_q = np.asarray(h) @ np.asarray(w_dq).T
+        q_c = (c_q @ np.asarray(w_uq).T).reshape(-1, H, dn)
+        w_qr = np.asarray(w_qr)
+        if w_qr.shape[1] != c_q.shape[1]:
+            return np.full(q_c.shape[:2] + (dn + dr,), np.nan)
+        q_r = (c_q @ w_qr.T).reshape(-1, H, dr)
+        return np.concatenate([q_c, q_r], axis=2)
+    monkeypatch.setattr(mla, "query_from_hidden", bad)
+    assert not _query_pins_pass()
+
+
+def test_planted_query_head_order(monkeypatch):
+    """W^QR rows taken head-interleaved instead of head-major."""
+    orig = mla.query_from_hidden
+
+    def bad(dims, h, w_dq, w_uq, w_qr):
+        H, dr = dims.n_heads, dims.d_rope
+        w2 = np.asarray(w_qr).reshape(dr, H, -1).transpose(1, 0, 2).reshape(H * dr, -1)
+        return orig(dims, h, w_dq, w_uq, w2)
+    monkeypatch.setattr(mla, "query_from_hidden", bad)
+    assert not _query_pins_pass()
+
+
+def test_planted_query_dropped_up_projection(monkeypatch):
+    """q^C = c^Q (W^UQ dropped) where the widths allow it."""
+    def bad(dims, h, w_dq, w_uq, w_qr):
+        H, dn, dr = dims.n_heads, dims.d_nope, dims.d_rope
+        c_q = np.asarray(h) @ np.asarray(w_dq).T
+        q_c = np.resize(c_q, (c_q.shape[0], H * dn)).reshape(-1, H, dn)
+        q_r = (np.asarray(h) @ np.asarray(w_qr).T).reshape(-1, H, dr)
+        return np.concatenate([q_c, q_r], axis=2)
+    monkeypatch.setattr(mla, "query_from_hidden", bad)
+    assert not _query_pins_pass()
+
+
+def test_planted_query_swapped_parts(monkeypatch):
+    """[q^R ; q^C] instead of [q^C ; q^R] per head."""
+    orig = mla.query_from_hidden
+
+    def bad(dims, h, w_dq, w_uq, w_qr):
+        q = orig(dims, h, w_dq, w_uq, w_qr)
+        return np.concatenate([q[..., dims.d_nope:], q[..., :dims.d_nope]], axis=2)[..., :q.shape[2]]
+    monkeypatch.setattr(mla, "query_from_hidden", bad)
+    assert not _query_pins_pass()
