@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--config", default="b128-l16k-t2",
                     choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2"])
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
+    ap.add_argument("--query-path", action="store_true",
+                    help="time the step from the hidden states alone (mla_layer_step: the "
+                         "query projections W^DQ, W^UQ, W^QR, then append and decode)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -99,7 +102,7 @@ def captured_traffic(config_key: str, kernel: str):
 
 
 # ----------------------------------------------------------------------------- work model
-def work_model(wl):
+def work_model(wl, query_path=False):
     """Algorithmic bytes and FLOPs per launch of each kernel, and per step."""
     d = wl.dims
     es = 2 if wl.dtype == "bf16" else 4
@@ -123,8 +126,16 @@ def work_model(wl):
     k["append_absorb"] = tuple(a + b for a, b in zip(k["compress_append"], k["absorb_q"]))
     tot_bytes = (R * D + H * dn * dc + H * dv * dc + D * H * dv) * es \
         + cache_rows * R * es + M * (D + H * (dn + dr) + D) * es
-    tot_flops = sum(k[n][1] for n in ("compress_append", "absorb_q", "attend", "value_proj",
-                                      "out_proj"))
+    steps = ["compress_append", "absorb_q", "attend", "value_proj", "out_proj"]
+    if query_path:
+        cq = d.d_cq
+        k["query_down"] = (cq * D * es + M * D * es + M * cq * es, 2.0 * M * cq * D)
+        k["query_rope"] = (H * dr * D * es + M * D * es + M * H * dr * es, 2.0 * M * H * dr * D)
+        k["query_up"] = (H * dn * cq * es + M * cq * es + M * H * dn * es, 2.0 * M * H * dn * cq)
+        # the queries are no longer an input: their weights are read instead
+        tot_bytes += (cq * D + H * dn * cq + H * dr * D) * es - M * H * (dn + dr) * es
+        steps += ["query_down", "query_rope", "query_up"]
+    tot_flops = sum(k[n][1] for n in steps)
     return k, tot_bytes, tot_flops, cache_rows * R * es
 
 
@@ -308,7 +319,8 @@ def run_mla(a, wl, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
     props = torch.cuda.get_device_properties(dev)
-    st = DeviceState(wl, device=local_rank)
+    st = DeviceState(wl, device=local_rank, query_path=a.query_path)
+    step = st.layer_step if a.query_path else st.step
     torch.cuda.synchronize()
     l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
     # L2 flush: write a 2x-L2 buffer, then read another one, so the timed step
@@ -322,7 +334,7 @@ def run_mla(a, wl, rank, local_rank, world):
         torch.sum(flush_r, dim=0, out=sink)
 
     for _ in range(a.warmup):
-        st.step()
+        step()
     torch.cuda.synchronize()
     if st.mla.check_status() != 0:
         raise RuntimeError("device status set during warm-up")
@@ -331,7 +343,7 @@ def run_mla(a, wl, rank, local_rank, world):
     n0 = st.mla.launch_count()
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
-        st.step()
+        step()
     launches_per_step = st.mla.launch_count() - n0
     for _ in range(a.warmup):
         flush()
@@ -378,7 +390,7 @@ def run_mla(a, wl, rank, local_rank, world):
     m.mla_profile_enable(st.mla.ctx, 1)
     g_prof = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_prof):
-        st.step()
+        step()
     kt = {}
     for i in range(a.steps):
         flush()
@@ -388,7 +400,7 @@ def run_mla(a, wl, rank, local_rank, world):
     m.mla_profile_enable(st.mla.ctx, 0)
 
     # ---- roofline of the dominant kernel and of the whole step
-    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl)
+    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path)
     avg = {k: sum(v) / len(v) for k, v in kt.items() if v}
     share = {k: sum(v) for k, v in kt.items()}
     dom = max(share, key=share.get)
@@ -423,7 +435,7 @@ def run_mla(a, wl, rank, local_rank, world):
 
         def e2e_step():
             st.step_inputs.copy_(in_h, non_blocking=True)
-            st.step()
+            step()
             out_h.copy_(st.out, non_blocking=True)
 
         g_e2e = torch.cuda.CUDAGraph()
@@ -463,12 +475,15 @@ def run_mla(a, wl, rank, local_rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) hidden states and queries, N(0,1/fan_in) weights",
-        "config": {"workload": wl.name, "batch": wl.B, "T": wl.T,
+        "config": {"workload": wl.name + ("+query-path" if a.query_path else ""),
+                   "batch": wl.B, "T": wl.T,
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
                    f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
                    "step's event bracket)",
-                   "graph": "each step is one CUDA-graph replay of mla_append_decode "
-                            "(append the new rows, then decode them)",
+                   "graph": ("each step is one CUDA-graph replay of mla_layer_step (queries "
+                             "from the new hidden states, append, decode)") if a.query_path else
+                            ("each step is one CUDA-graph replay of mla_append_decode "
+                             "(append the new rows, then decode them)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cache_gbs": cache_bytes / t_step / 1e9,
                    "step_algorithmic_gb": tot_bytes / 1e9,

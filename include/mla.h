@@ -79,15 +79,27 @@ typedef struct {
   float softmax_scale;
   float rope_base;
   mla_dtype dtype;
+  /* Width d_c' of the query latent c^Q = W^DQ h, for mla_layer_step; 0 when
+   * the context decodes from given queries only.  The pages give no value.
+   * bf16 contexts need a multiple of 128 (<= 16384); fp32 any width
+   * <= 4096. */
+  int d_cq;
 } mla_config;
 
-/* Device pointers to the five projection matrices (layouts above). */
+/* Device pointers to the projection matrices (layouts above).  The last
+ * three (query path, mla_layer_step) are read only when d_cq > 0:
+ *      w_dq [d_cq, d_model]   w_uq [n_heads*d_nope, d_cq]
+ *      w_qr [n_heads*d_rope, d_model]
+ * head i owning rows i*d_nope.. of w_uq and i*d_rope.. of w_qr. */
 typedef struct {
   const void* w_dkv;
   const void* w_kr;
   const void* w_uk;
   const void* w_uv;
   const void* w_o;
+  const void* w_dq;
+  const void* w_uq;
+  const void* w_qr;
 } mla_weights;
 
 typedef struct mla_ctx mla_ctx;
@@ -157,6 +169,25 @@ mla_status mla_append_decode(mla_ctx* ctx, const void* h, const int32_t* positio
                              const int32_t* block_table, int max_pages,
                              const int32_t* seq_lens, int batch, int T, void* out,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step of the attention layer from the hidden states alone:
+ * the query path, then mla_append_decode.  The query of new token t of
+ * sequence b comes from its hidden state h_t (the row appended to the
+ * cache) as the pages give it (liang.world ch.2 §2, last paragraph: the
+ * query's own low-rank compression c^Q; tuntang.top, "RoPE 的兼容性处理":
+ * q_t = [W^UQ c_t^Q ; W^QR h_t . RoPE(t)]):
+ *   c^Q = W^DQ h,  q^C_i = (W^UQ c^Q)_i,  q^R_i = (W^QR h)_i rotated at the
+ *   token's position,
+ * then q_i = [q^C_i ; q^R_i] is decoded as by mla_decode.  W^UK is folded
+ * into the query after W^UQ (the same absorption as mla_decode).
+ * Arguments, layouts, ownership and errors are those of mla_append_decode
+ * without `q`; the context needs d_cq > 0 (else MLA_ERR_UNSUPPORTED), and
+ * the workspace (mla_decode_workspace_size) then also holds c^Q and q. */
+mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
+                          void* cache, int num_pages, const int32_t* block_table,
+                          int max_pages, const int32_t* seq_lens, int batch,
+                          int T, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* Decode without a workspace argument, for callers that cannot allocate
  * device memory when they decode (a fixed memory budget reserved up front,

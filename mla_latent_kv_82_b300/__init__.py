@@ -29,7 +29,7 @@ EXPORTED = (
     "mla_create", "mla_destroy", "mla_compress_append", "mla_decode_workspace_size",
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
-    "mla_decode_static_workspace", "mla_append_decode",
+    "mla_decode_static_workspace", "mla_append_decode", "mla_layer_step",
 )
 
 
@@ -39,14 +39,15 @@ class mla_config(ctypes.Structure):
         ("d_v", ctypes.c_int), ("d_latent", ctypes.c_int), ("d_rope", ctypes.c_int),
         ("page_size", ctypes.c_int), ("max_position", ctypes.c_int),
         ("softmax_scale", ctypes.c_float), ("rope_base", ctypes.c_float),
-        ("dtype", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("d_cq", ctypes.c_int),
     ]
 
 
 class mla_weights(ctypes.Structure):
     _fields_ = [("w_dkv", ctypes.c_void_p), ("w_kr", ctypes.c_void_p),
                 ("w_uk", ctypes.c_void_p), ("w_uv", ctypes.c_void_p),
-                ("w_o", ctypes.c_void_p)]
+                ("w_o", ctypes.c_void_p), ("w_dq", ctypes.c_void_p),
+                ("w_uq", ctypes.c_void_p), ("w_qr", ctypes.c_void_p)]
 
 
 class MLAError(RuntimeError):
@@ -78,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode_static_workspace": ([vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp], i32),
         "mla_append_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp],
                               i32),
+        "mla_layer_step": ([vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp], i32),
         "mla_profile_read": ([vp, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_char_p), i32], i32),
     }
@@ -136,6 +138,12 @@ def mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_p
                                   seq_lens, batch, T, out, workspace, workspace_bytes, stream)
 
 
+def mla_layer_step(ctx, h, positions, cache, num_pages, block_table, max_pages, seq_lens, batch,
+                   T, out, workspace, workspace_bytes, stream) -> int:
+    return _lib.mla_layer_step(ctx, h, positions, cache, num_pages, block_table, max_pages,
+                               seq_lens, batch, T, out, workspace, workspace_bytes, stream)
+
+
 def mla_decode_static_workspace(ctx, q, cache, num_pages, block_table, max_pages, seq_lens,
                                 batch, T, out, stream) -> int:
     """mla_decode with the library's static scratch instead of a workspace
@@ -190,9 +198,11 @@ class MLA:
         cfg = mla_config(dims.d_model, dims.n_heads, dims.d_nope, dims.d_v, dims.d_latent,
                          dims.d_rope, dims.page_size, max_position,
                          softmax_scale if softmax_scale is not None else dims.softmax_scale,
-                         dims.rope_base, MLA_BF16 if dtype == "bf16" else MLA_FP32)
-        w = mla_weights(*(self.weights[k].data_ptr() for k in
-                          ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o")))
+                         dims.rope_base, MLA_BF16 if dtype == "bf16" else MLA_FP32,
+                         getattr(dims, "d_cq", 0))
+        names = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o", "w_dq", "w_uq", "w_qr")
+        w = mla_weights(*(self.weights[k].data_ptr() if k in self.weights else None
+                          for k in names))
         st, self.ctx = mla_create(cfg, w, device)
         if st != MLA_OK:
             raise MLAError(st, "mla_create")
@@ -237,6 +247,17 @@ class MLA:
                                self._stream(stream))
         if st != MLA_OK:
             raise MLAError(st, "mla_append_decode")
+
+    def layer_step(self, h, positions, cache, block_table, seq_lens, out, workspace,
+                   stream=None):
+        batch, T = out.shape[0], out.shape[1]
+        st = mla_layer_step(self.ctx, h.data_ptr(), positions.data_ptr(), cache.data_ptr(),
+                            cache.shape[0] // self.dims.page_size, block_table.data_ptr(),
+                            block_table.shape[-1], seq_lens.data_ptr(), batch, T, out.data_ptr(),
+                            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                            self._stream(stream))
+        if st != MLA_OK:
+            raise MLAError(st, "mla_layer_step")
 
     def check_status(self, stream=None) -> int:
         return mla_check_status(self.ctx, self._stream(stream))

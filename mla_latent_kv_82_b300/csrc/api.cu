@@ -32,6 +32,9 @@ mla_status validate_config(const mla_config* c) {
   if (!(c->softmax_scale > 0.f) || !std::isfinite(c->softmax_scale)) return MLA_ERR_INVALID_ARG;
   if (!(c->rope_base > 1.f) || !std::isfinite(c->rope_base)) return MLA_ERR_INVALID_ARG;
   if (c->max_position > (1 << 26)) return MLA_ERR_UNSUPPORTED;
+  if (c->d_cq < 0) return MLA_ERR_INVALID_ARG;
+  if (c->d_cq > (c->dtype == MLA_BF16 ? 16384 : 4096)) return MLA_ERR_UNSUPPORTED;
+  if (c->dtype == MLA_BF16 && c->d_cq % 128 != 0) return MLA_ERR_UNSUPPORTED;
   if (c->dtype == MLA_BF16) {
     if (c->n_heads != 128 || c->d_nope != 128 || c->d_v != 128 || c->d_latent != 512 ||
         c->d_rope != 64 || c->page_size != 64 || c->d_model % 128 != 0 || c->d_model > 16384)
@@ -94,6 +97,9 @@ mla_status mla_create(const mla_config* cfg, const mla_weights* w, int device, m
   const size_t align = cfg->dtype == MLA_BF16 ? 16 : 4;
   if (!aligned(w->w_dkv, align) || !aligned(w->w_kr, align) || !aligned(w->w_uk, align) ||
       !aligned(w->w_uv, align) || !aligned(w->w_o, align))
+    return MLA_ERR_INVALID_ARG;
+  if (cfg->d_cq > 0 && (!w->w_dq || !w->w_uq || !w->w_qr || !aligned(w->w_dq, align) ||
+                        !aligned(w->w_uq, align) || !aligned(w->w_qr, align)))
     return MLA_ERR_INVALID_ARG;
   if (device < 0) return MLA_ERR_INVALID_ARG;
   int ndev = 0;
@@ -272,6 +278,51 @@ mla_status mla_append_decode(mla_ctx* ctx, const void* h, const int32_t* positio
     mla::f32_decode(ctx, static_cast<const float*>(q), static_cast<const float*>(cache),
                     num_pages, block_table, max_pages, batch, T, static_cast<float*>(out), ws,
                     L, st);
+  }
+  mla::prof_mark(ctx, st, nullptr);
+  if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  return launch_status();
+}
+
+mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions, void* cache,
+                          int num_pages, const int32_t* block_table, int max_pages,
+                          const int32_t* seq_lens, int batch, int T, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!ctx || !h || !positions || !cache || !block_table || !seq_lens || !out || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (ctx->cfg.d_cq <= 0) return MLA_ERR_UNSUPPORTED;
+  if (batch < 1 || T < 1 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (T > 8 || (long long)batch * max_pages > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+  const size_t a = ctx->cfg.dtype == MLA_BF16 ? 16 : 4;
+  if (!aligned(h, a) || !aligned(cache, a) || !aligned(out, a) || !aligned(workspace, 256) ||
+      !aligned(positions, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  const mla::WsLayout L = mla::workspace_layout(ctx, batch, T, max_pages);
+  if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int M = batch * T;
+  bool launched = true;
+  if (ctx->cfg.dtype == MLA_BF16) {
+    const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+    launched = mla::bf16_query(ctx, hb, M, ws, L, st) &&
+               mla::bf16_append_decode(
+                   ctx, hb, positions, reinterpret_cast<const __nv_bfloat16*>(ws + L.q_in),
+                   static_cast<__nv_bfloat16*>(cache), num_pages, block_table, max_pages, seq_lens,
+                   batch, T, static_cast<__nv_bfloat16*>(out), ws, L, st);
+  } else {
+    const float* hf = static_cast<const float*>(h);
+    mla::f32_query(ctx, hf, M, ws, L, st);
+    mla::f32_compress_append(ctx, hf, batch, T, positions, block_table, max_pages,
+                             static_cast<float*>(cache), num_pages, st);
+    mla::prof_mark(ctx, st, "plan");
+    mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
+    ctx->launches += 1;
+    mla::f32_decode(ctx, reinterpret_cast<const float*>(ws + L.q_in),
+                    static_cast<const float*>(cache), num_pages, block_table, max_pages, batch, T,
+                    static_cast<float*>(out), ws, L, st);
   }
   mla::prof_mark(ctx, st, nullptr);
   if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }

@@ -180,16 +180,28 @@ GemmShape gemm_shape(const mla_ctx* ctx, int M, int m_tiles, int k_chunks, int m
 
 struct Bf16Plans {
   GemmShape abs, uv, o;
+  GemmShape dq, uq, qr;   // query path (d_cq > 0)
 };
 
+constexpr size_t kSplitCap = 64u << 20;   // bound on the split-K scratch of the largest-M cases
+
 Bf16Plans decode_plans(const mla_ctx* ctx, int M) {
-  const size_t cap = 64u << 20;   // bound on the split-K scratch of the largest-M cases
+  const int D = ctx->cfg.d_model, dcq = ctx->cfg.d_cq;
   Bf16Plans p;
   p.abs = gemm_shape(ctx, M, kHeads * (kLat / 128), kNope / 64, 4, 0);
   p.abs.splits = 1;   // two K chunks only: never split
-  p.uv = gemm_shape(ctx, M, kHeads, kLat / 64, 4, cap);
-  p.o = gemm_shape(ctx, M, ctx->cfg.d_model / 128, kHeads * kDv / 64, 4, cap);
+  p.uv = gemm_shape(ctx, M, kHeads, kLat / 64, 4, kSplitCap);
+  p.o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap);
+  if (dcq > 0) {
+    p.dq = gemm_shape(ctx, M, dcq / 128, D / 64, 4, kSplitCap);
+    p.uq = gemm_shape(ctx, M, kHeads, dcq / 64, 4, kSplitCap);
+    p.qr = gemm_shape(ctx, M, kHeads * kRope / 128, D / 64, 4, kSplitCap);
+  }
   return p;
+}
+
+size_t partial_bytes(const GemmShape& g, int m_tiles) {
+  return (size_t)m_tiles * g.n_tiles * g.splits * g.nt * 128 * sizeof(float);
 }
 
 WgArgs base_args(const mla_ctx* ctx) {
@@ -213,10 +225,13 @@ bool check(cudaError_t e) {
 
 size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M) {
   const Bf16Plans p = decode_plans(ctx, M);
-  const size_t uv = (size_t)kHeads * p.uv.n_tiles * p.uv.splits * p.uv.nt * 128 * sizeof(float);
-  const size_t o = (size_t)(ctx->cfg.d_model / 128) * p.o.n_tiles * p.o.splits * p.o.nt * 128 *
-                   sizeof(float);
-  return std::max(uv, o);
+  size_t b = std::max(partial_bytes(p.uv, kHeads), partial_bytes(p.o, ctx->cfg.d_model / 128));
+  if (ctx->cfg.d_cq > 0) {
+    b = std::max(b, partial_bytes(p.dq, ctx->cfg.d_cq / 128));
+    b = std::max(b, partial_bytes(p.uq, kHeads));
+    b = std::max(b, partial_bytes(p.qr, kHeads * kRope / 128));
+  }
+  return b;
 }
 
 bool bf16_setup(mla_ctx* ctx) {
@@ -227,7 +242,14 @@ bool bf16_setup(mla_ctx* ctx) {
             make_tmap_bf16_2d(&ctx->tm_wuk, w.w_uk, kHeads * kNope, kLat, kLat, 64, 64, true) &&
             make_tmap_bf16_2d(&ctx->tm_wuv, w.w_uv, kHeads * kDv, kLat, kLat, 64, 128, true) &&
             make_tmap_bf16_2d(&ctx->tm_wo, w.w_o, D, kHeads * kDv, kHeads * kDv, 64, 128, true);
+  if (ok && ctx->cfg.d_cq > 0) {
+    const int dcq = ctx->cfg.d_cq;
+    ok = make_tmap_bf16_2d(&ctx->tm_wdq, w.w_dq, dcq, D, D, 64, 128, true) &&
+         make_tmap_bf16_2d(&ctx->tm_wuq, w.w_uq, kHeads * kNope, dcq, dcq, 64, 128, true) &&
+         make_tmap_bf16_2d(&ctx->tm_wqr, w.w_qr, kHeads * kRope, D, D, 64, 128, true);
+  }
   if (!ok) return false;
+  if (!sv_setup(ctx)) return false;
   if (cudaMalloc(&ctx->append_partials, kAppendPartialBytes) != cudaSuccess ||
       cudaMalloc(&ctx->counters, kCounters * sizeof(int)) != cudaSuccess ||
       cudaMemset(ctx->counters, 0, kCounters * sizeof(int)) != cudaSuccess) {
@@ -349,10 +371,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     }
   }
   // ---- split-KV attention over the latent cache
-  const bool paired = T % 2 == 0;   // tokens 2j, 2j+1 share every cache tile
-  if (!(paired ? tc_attend_pair : tc_attend)(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws,
-                                             L, st))
-    return false;
+  if (!sv_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) return false;
   // ---- log-sum-exp combine -> o_lat (bf16)
   {
     prof_mark(ctx, st, "combine");
@@ -442,6 +461,61 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     if (!check(wgemm_launch(p, WG_ROWMAJOR, false, st, true))) return false;
   }
   return true;
+}
+
+// Query path: c^Q = W^DQ h, q^R = W^QR h (row r of W^QR is feature r % 64 of
+// head r / 64), q^C = W^UQ c^Q, written as mla_decode's q [M, heads, 192].
+bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsLayout& L,
+                cudaStream_t st) {
+  const int D = ctx->cfg.d_model, dcq = ctx->cfg.d_cq;
+  const Bf16Plans bp = decode_plans(ctx, M);
+  if (bp.dq.n_tiles > 65535 || bp.uq.n_tiles > 65535 || bp.qr.n_tiles > 65535) return false;
+  __nv_bfloat16* cq = reinterpret_cast<__nv_bfloat16*>(ws + L.c_q);
+  __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(ws + L.q_in);
+  float* part = reinterpret_cast<float*>(ws + L.wg_part);
+  constexpr int kQRow = kHeads * (kNope + kRope);
+  auto rowmajor = [&](const GemmShape& g, int m_tiles, const CUtensorMap& wmap, const void* x,
+                      int x_cols, int k_chunks, int tiles_per_head, int a_head_rows,
+                      __nv_bfloat16* out, int ld_out, int out_head_cols, int rows_per_head,
+                      const char* name) {
+    WgPlan p{};
+    p.nt = g.nt;
+    p.n_tiles = g.n_tiles;
+    p.m_tiles = m_tiles;
+    p.tmA = wmap;
+    p.tmA2 = wmap;
+    if (!make_tmap_bf16_2d(&p.tmB, x, M, x_cols, x_cols, 64, p.nt, false)) {
+      cudaGetLastError();
+      return false;
+    }
+    WgArgs& a = p.args;
+    a = base_args(ctx);
+    a.n_tokens = M;
+    a.k_chunks = k_chunks;
+    a.splits = g.splits;
+    a.tiles_per_head = tiles_per_head;
+    a.a_head_rows = a_head_rows;
+    a.b_head_cols = 0;
+    a.out = out;
+    a.ld_out = ld_out;
+    a.out_head_cols = out_head_cols;
+    a.out_rows_per_head = rows_per_head;
+    a.partials = part;
+    prof_mark(ctx, st, name);
+    ctx->launches += 1;
+    return check(wgemm_launch(p, WG_ROWMAJOR, false, st, true));
+  };
+  // c^Q [M, d_cq]
+  if (!rowmajor(bp.dq, dcq / 128, ctx->tm_wdq, h, D, D / 64, dcq / 128, 0, cq, dcq, 0, 0,
+                "query_down"))
+    return false;
+  // q^R (un-rotated) -> q[:, head, 128..191]
+  if (!rowmajor(bp.qr, kHeads * kRope / 128, ctx->tm_wqr, h, D, D / 64, kHeads * kRope / 128, 0,
+                q + kNope, kQRow, kNope + kRope, kRope, "query_rope"))
+    return false;
+  // q^C -> q[:, head, 0..127]
+  return rowmajor(bp.uq, kHeads, ctx->tm_wuq, cq, dcq, dcq / 64, 1, kNope, q, kQRow,
+                  kNope + kRope, 0, "query_up");
 }
 
 bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos,

@@ -22,8 +22,12 @@ struct mla_ctx {
   int64_t launches;
   // bf16 path: TMA maps of the weights, split-K scratch of the append
   CUtensorMap tm_wdkv, tm_wkr, tm_wuk, tm_wuv, tm_wo;
+  CUtensorMap tm_wdq, tm_wuq, tm_wqr;   // query path (d_cq > 0)
   float* append_partials = nullptr;   // kAppendPartialBytes
   int* counters = nullptr;            // kCounters, zero between launches
+  // attention clusters that fit on the device at once: [0] two-CTA clusters
+  // (odd T), [1] four-CTA clusters (even T)
+  int sv_clusters[2] = {0, 0};
   // per-kernel timing (mla_profile_enable)
   bool prof = false;
   int n_marks = 0;
@@ -47,7 +51,9 @@ struct WsLayout {
   size_t part_lse; // fp32 [n_slots, T, n_heads] (log2 domain)
   size_t o_lat;    // dtype [batch*T, n_heads, d_latent]
   size_t o;        // dtype [batch*T, n_heads*d_v]
-  size_t wg_part;  // fp32 split-K partials of the value / output projections
+  size_t wg_part;  // fp32 split-K partials of the projections
+  size_t c_q;      // query path (d_cq > 0): dtype [batch*T, d_cq]
+  size_t q_in;     // query path: dtype [batch*T, n_heads, d_nope + d_rope]
   size_t total;
 };
 
@@ -86,18 +92,24 @@ bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos
                         const int32_t* bt, int max_pages, const int32_t* seq_lens, int B, int T,
                         __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
 
+// Query path of mla_layer_step: q = [W^UQ W^DQ h ; W^QR h] per head into
+// the workspace's q_in (layout of mla_decode's q).
+bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsLayout& L,
+                cudaStream_t st);
+void f32_query(mla_ctx* ctx, const float* h, int M, char* ws, const WsLayout& L,
+               cudaStream_t st);
+
 // bf16 path helpers
 bool bf16_setup(mla_ctx* ctx);                 // weight maps + scratch, at create
 void bf16_teardown(mla_ctx* ctx);
 size_t bf16_wg_partial_bytes(const mla_ctx* ctx, int M);
-bool tc_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
+// Split-KV attention over the latent cache (attend_sv.cu): one cluster per
+// (KV split, query token) for odd T, per (KV split, token pair) for even T.
+bool sv_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
                int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
                const WsLayout& L, cudaStream_t st);
-// Same contract for an even T: query tokens 2j, 2j+1 share each cache tile on a
-// CTA pair (cta_group::2).
-bool tc_attend_pair(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cache,
-               int num_pages, const int32_t* bt, int max_pages, int B, int T, char* ws,
-               const WsLayout& L, cudaStream_t st);
+// Fills ctx->sv_clusters (at context creation).
+bool sv_setup(mla_ctx* ctx);
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
 

@@ -58,8 +58,11 @@ static int choose_splits(const mla_ctx* ctx, int B, int T, int max_pages) {
   const long long pages_bound = (long long)B * max_pages;
   int G;
   if (ctx->cfg.dtype == MLA_BF16) {
-    // one CTA per (split, query token, half of d_latent), one CTA per SM
+    // one cluster of two CTAs per (split, query token) for odd T, of four
+    // per (split, token pair) for even T, one CTA per SM, all resident at once
     G = ctx->num_sms / (2 * T);
+    const int fit = T % 2 ? ctx->sv_clusters[0] / T : ctx->sv_clusters[1] / (T / 2);
+    if (fit >= 1 && fit < G) G = fit;
   } else {
     const int groups = (ctx->cfg.n_heads + 7) / 8;
     G = (2 * ctx->num_sms + T * groups - 1) / (T * groups);
@@ -90,6 +93,10 @@ WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages) {
   L.o_lat = take(es * M * c.n_heads * c.d_latent);
   L.o = take(es * M * c.n_heads * c.d_v);
   L.wg_part = take(c.dtype == MLA_BF16 ? bf16_wg_partial_bytes(ctx, (int)M) : 0);
+  if (c.d_cq > 0) {
+    L.c_q = take(es * M * c.d_cq);
+    L.q_in = take(es * M * c.n_heads * (c.d_nope + c.d_rope));
+  }
   L.total = off;
   return L;
 }

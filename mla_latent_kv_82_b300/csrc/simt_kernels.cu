@@ -28,11 +28,13 @@ struct AppendArgs {
 
 // C[m, n] = sum_k A[m, k] * B[n, k], B's rows n < n_split from B0, the rest
 // from B1 (row n - n_split).  fp32 accumulation.  64x64 tiles, 4x4 per thread.
+// EPI_STORE writes C[m, n] at m * ldc + (n / col_group) * col_stride +
+// n % col_group (col_group = N, col_stride = 0: plain row-major).
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kGemmThreads)
 gemm_tn_kernel(int M, int N, int K, const T* __restrict__ A, int lda,
                const T* __restrict__ B0, const T* __restrict__ B1, int n_split, int ldb,
-               T* __restrict__ C, int ldc, AppendArgs ap) {
+               T* __restrict__ C, int ldc, AppendArgs ap, int col_group, int col_stride) {
   __shared__ float As[kTK][kTM + 4];
   __shared__ float Bs[kTK][kTN + 4];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -73,8 +75,12 @@ gemm_tn_kernel(int M, int N, int K, const T* __restrict__ A, int lda,
     const int nb = n0 + tx * 4;
     if (MODE == EPI_STORE) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (nb + j < N) C[(size_t)m * ldc + nb + j] = from_f<T>(acc[i][j]);
+      for (int j = 0; j < 4; ++j) {
+        const int n = nb + j;
+        if (n < N)
+          C[(size_t)m * ldc + (size_t)(n / col_group) * col_stride + n % col_group] =
+              from_f<T>(acc[i][j]);
+      }
     } else {
       // compress + RoPE + paged append of token m
       const int pos = ap.pos[m];
@@ -285,7 +291,32 @@ void compress_append_impl(mla_ctx* ctx, const T* h, int B, int T_, const int32_t
   ctx->launches += 1;
   gemm_tn_kernel<T, EPI_APPEND><<<grid, kGemmThreads, 0, st>>>(
       M, N, K, h, K, static_cast<const T*>(ctx->w.w_dkv), static_cast<const T*>(ctx->w.w_kr),
-      c.d_latent, K, cache, N, ap);
+      c.d_latent, K, cache, N, ap, N, 0);
+}
+
+// q = [W^UQ W^DQ h ; W^QR h] per head, in mla_decode's q layout.
+template <typename T>
+void query_impl(mla_ctx* ctx, const T* h, int M, char* ws, const WsLayout& L, cudaStream_t st) {
+  const mla_config& c = ctx->cfg;
+  const int H = c.n_heads, dn = c.d_nope, dr = c.d_rope, D = c.d_model, dcq = c.d_cq;
+  T* cq = reinterpret_cast<T*>(ws + L.c_q);
+  T* q = reinterpret_cast<T*>(ws + L.q_in);
+  AppendArgs none{};
+  auto grid = [&](int N) { return dim3((N + kTN - 1) / kTN, (M + kTM - 1) / kTM); };
+  prof_mark(ctx, st, "query_down");
+  ctx->launches += 1;
+  gemm_tn_kernel<T, EPI_STORE><<<grid(dcq), kGemmThreads, 0, st>>>(
+      M, dcq, D, h, D, static_cast<const T*>(ctx->w.w_dq), nullptr, dcq, D, cq, dcq, none, dcq, 0);
+  prof_mark(ctx, st, "query_rope");
+  ctx->launches += 1;
+  gemm_tn_kernel<T, EPI_STORE><<<grid(H * dr), kGemmThreads, 0, st>>>(
+      M, H * dr, D, h, D, static_cast<const T*>(ctx->w.w_qr), nullptr, H * dr, D, q + dn,
+      H * (dn + dr), none, dr, dn + dr);
+  prof_mark(ctx, st, "query_up");
+  ctx->launches += 1;
+  gemm_tn_kernel<T, EPI_STORE><<<grid(H * dn), kGemmThreads, 0, st>>>(
+      M, H * dn, dcq, cq, dcq, static_cast<const T*>(ctx->w.w_uq), nullptr, H * dn, dcq, q,
+      H * (dn + dr), none, dn, dn + dr);
 }
 
 template <typename T>
@@ -325,7 +356,7 @@ void decode_impl(mla_ctx* ctx, const T* q, const T* cache, int num_pages,
   ctx->launches += 1;
   gemm_tn_kernel<T, EPI_STORE><<<dim3((N + kTN - 1) / kTN, (M + kTM - 1) / kTM), kGemmThreads, 0,
                                  st>>>(M, N, K, o, K, static_cast<const T*>(ctx->w.w_o), nullptr,
-                                       N, K, out, N, none);
+                                       N, K, out, N, none, N, 0);
 }
 
 }  // namespace
@@ -334,6 +365,11 @@ void f32_compress_append(mla_ctx* ctx, const float* h, int B, int T, const int32
                          const int32_t* bt, int max_pages, float* cache, int num_pages,
                          cudaStream_t st) {
   compress_append_impl<float>(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, st);
+}
+
+void f32_query(mla_ctx* ctx, const float* h, int M, char* ws, const WsLayout& L,
+               cudaStream_t st) {
+  query_impl<float>(ctx, h, M, ws, L, st);
 }
 
 void f32_decode(mla_ctx* ctx, const float* q, const float* cache, int num_pages,

@@ -250,7 +250,12 @@ __device__ __forceinline__ void wgemm_body(const CUtensorMap& tmA, const CUtenso
           if (t >= a.n_tokens || ch * 8 >= rows_valid) continue;
           const uint4 val = *reinterpret_cast<const uint4*>(stg + j * kStgPitch + ch * 8);
           __nv_bfloat16* dst = nullptr;
-          if (EPI == WG_ROWMAJOR) {
+          if (EPI == WG_ROWMAJOR && a.out_rows_per_head > 0) {
+            // weight row gr belongs to output head gr / rows_per_head
+            const int gr = tile * 128 + ch * 8;
+            dst = a.out + (size_t)t * a.ld_out + (gr / a.out_rows_per_head) * a.out_head_cols +
+                  gr % a.out_rows_per_head;
+          } else if (EPI == WG_ROWMAJOR) {
             dst = a.out + (size_t)t * a.ld_out + head * a.out_head_cols + tile * 128 + ch * 8;
           } else if (EPI == WG_QIMG) {
             // 8 consecutive features of one head are one 16-byte chunk of the image

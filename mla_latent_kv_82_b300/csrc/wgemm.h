@@ -21,9 +21,12 @@ struct WgArgs {
   int a_head_rows;       // A row offset per head
   int b_head_cols;       // B column offset per head
   int valid_rows_last;   // rows written for the last tile of a head
-  // WG_ROWMAJOR: out[t * ld_out + head * out_head_cols + tile * 128 + f]
+  // WG_ROWMAJOR: out[t * ld_out + head * out_head_cols + tile * 128 + f]; with
+  // out_rows_per_head > 0 instead weight row r = tile * 128 + f (head 0) goes
+  // to out[t * ld_out + (r / out_rows_per_head) * out_head_cols +
+  // r % out_rows_per_head] (several output heads per weight tile)
   __nv_bfloat16* out;
-  int ld_out, out_head_cols;
+  int ld_out, out_head_cols, out_rows_per_head;
   // WG_APPEND: cache row of token t; RoPE on rows of tile append_rope_tile
   __nv_bfloat16* cache;
   const int32_t* pos;

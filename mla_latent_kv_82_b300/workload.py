@@ -5,26 +5,34 @@ Builds everything a decode step needs on one GPU from a seeded
 weights and queries come from the seeded generator (on the device), the
 pool is prefilled by chunked ``mla_compress_append`` calls, and ``step()``
 is one pass of the hot path: append the T new tokens of every sequence,
-then decode them.
+then decode them.  With ``query_path`` the context also holds the query
+projections and ``layer_step()`` makes the same step from the hidden states
+alone (the queries come from the new tokens' hidden states).
 """
 from __future__ import annotations
+
+import dataclasses
 
 import torch
 
 from . import MLA
 
 W_NAMES = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o")
+Q_NAMES = ("w_dq", "w_uq", "w_qr")
 
 
 class DeviceState:
     def __init__(self, wl, device: int = 0, prefill: bool = True, chunk: int = 32768,
-                 sentinel: float | None = None, block_table=None):
+                 sentinel: float | None = None, block_table=None, query_path: bool = False):
         self.wl = wl
         self.dev = torch.device("cuda", device)
         d = wl.dims
         dt = wl.torch_dtype
-        self.weights = {n: wl.weight(n, device=self.dev) for n in W_NAMES}
-        self.mla = MLA(d, self.weights, wl.dtype, max_position=max(wl.seq_lens), device=device)
+        names = W_NAMES + (Q_NAMES if query_path else ())
+        self.weights = {n: wl.weight(n, device=self.dev) for n in names}
+        ctx_dims = d if query_path else dataclasses.replace(d, d_cq=0)
+        self.mla = MLA(ctx_dims, self.weights, wl.dtype, max_position=max(wl.seq_lens),
+                       device=device)
         bt = wl.block_table() if block_table is None else block_table
         self.bt = torch.as_tensor(bt, dtype=torch.int32, device=self.dev).contiguous()
         self.num_pages = int(self.bt.max().item()) + 1
@@ -84,6 +92,12 @@ class DeviceState:
         mla_append_decode call)."""
         self.mla.append_decode(self.h_new, self.pos_new, self.q, self.cache, self.bt,
                                self.seq_lens, self.out, self.ws, stream=stream)
+
+    def layer_step(self, stream=None):
+        """The step from the hidden states alone (mla_layer_step): the query
+        path makes the queries of the new tokens, then append and decode."""
+        self.mla.layer_step(self.h_new, self.pos_new, self.cache, self.bt, self.seq_lens,
+                            self.out, self.ws, stream=stream)
 
     def step_separate(self, stream=None):
         """The same step as two calls: mla_compress_append, then mla_decode."""

@@ -11,7 +11,8 @@ d = 5120, n_h = 128, d_h = 128, d_c = 512, d_h^R = 64); the tiny fp32 case
 uses n_h = 4, d_c = 32, d_R = 8, d_h = 16, d = 64.
 
 Recipe (every value is seeded):
-* tensor ids: h=0, W^DKV=1, W^KR=2, W^UK=3, W^UV=4, W_O=5, q=6;
+* tensor ids: h=0, W^DKV=1, W^KR=2, W^UK=3, W^UV=4, W_O=5, q=6, and for the
+  query path W^DQ=7, W^UQ=8, W^QR=9;
 * h and q ~ N(0, 1); every weight ~ N(0, 1/fan_in), fan_in = input width;
 * sequence b has ``lens[b]`` cached tokens before the step and ``T`` new
   tokens; h of token p of sequence b is row ``b * row_stride + p`` of a
@@ -32,7 +33,7 @@ import torch
 
 from . import gen
 
-TID_H, TID_WDKV, TID_WKR, TID_WUK, TID_WUV, TID_WO, TID_Q = range(7)
+TID_H, TID_WDKV, TID_WKR, TID_WUK, TID_WUV, TID_WO, TID_Q, TID_WDQ, TID_WUQ, TID_WQR = range(10)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -45,6 +46,7 @@ class Dims:
     d_rope: int
     page_size: int
     rope_base: float = 10000.0
+    d_cq: int = 0          # width of the query latent c^Q (query path); not on the pages
 
     @property
     def row_width(self) -> int:
@@ -58,9 +60,9 @@ class Dims:
 
 
 V2 = Dims(d_model=5120, n_heads=128, d_nope=128, d_v=128, d_latent=512,
-          d_rope=64, page_size=64)
+          d_rope=64, page_size=64, d_cq=1536)
 TINY = Dims(d_model=64, n_heads=4, d_nope=16, d_v=16, d_latent=32,
-            d_rope=8, page_size=64)
+            d_rope=8, page_size=64, d_cq=48)
 
 
 @dataclasses.dataclass
@@ -123,6 +125,9 @@ class Workload:
             "w_uk": (TID_WUK, (d.n_heads * d.d_nope, d.d_latent), d.d_latent),
             "w_uv": (TID_WUV, (d.n_heads * d.d_v, d.d_latent), d.d_latent),
             "w_o": (TID_WO, (d.d_model, d.n_heads * d.d_v), d.n_heads * d.d_v),
+            "w_dq": (TID_WDQ, (d.d_cq, d.d_model), d.d_model),
+            "w_uq": (TID_WUQ, (d.n_heads * d.d_nope, d.d_cq), d.d_cq),
+            "w_qr": (TID_WQR, (d.n_heads * d.d_rope, d.d_model), d.d_model),
         }[name]
         tid, shape, fan_in = spec
         return gen.fill(self.seed, tid, shape, 1.0 / math.sqrt(fan_in),

@@ -1,18 +1,24 @@
 """Model of the attention kernel's barrier protocol (CPU only).
 
-The split-KV attention kernel runs five roles that meet only at mbarriers:
-a TMA producer, a score-MMA issuer, a value-MMA issuer, the softmax warps
-and (implicitly) the tensor pipe.  Every wait is a parity wait, which cannot
-tell phase F from phase F + 2.  This file restates each role's loop (the
-order of its waits and arrivals, nothing of the arithmetic) and drives the
-roles in many interleavings over the split plans of the five workloads.  A
-wait that passes while its barrier is not exactly at the awaited phase is a
-failure, and so is a state where no role can move.
+The split-KV attention kernel (attend_sv.cu) runs, per cluster, a score side
+(TMA producer, score-MMA issuer, softmax warps) and a value side (TMA
+producer, value-MMA issuer, correction/epilogue warps, and for token pairs a
+relay warp in the odd value CTA).  They meet only at mbarriers, and every
+wait is a parity wait, which cannot tell phase F from phase F + 2.
 
-Copies, MMAs and commits complete as soon as they are issued: they never
-wait on anything once issued, so this can only hide delays, not orderings.
-The model follows the kernel's loops one for one; a change to the order of
-waits or arrivals in the kernel must be made here too.
+This file restates each role's loop (the order of its waits, arrivals and
+buffer accesses, nothing of the arithmetic) and drives the roles in many
+random interleavings over the split plans of the workloads.  Besides
+deadlock and a parity wait passing on the wrong phase, it tracks what every
+buffer holds and fails when a role reads a buffer that does not hold what
+it expects: a ring slot (stage number), an S buffer (tile), a landing buffer
+(tile), q~ and the RoPE block (segment), and O (which value MMAs, rescales
+and read-outs have happened).
+
+Copies complete in random order, and only when a separate copy-engine role
+runs; MMAs complete when issued (they wait on nothing once issued), so this
+can only hide delays, not orderings.  A change to the order of waits,
+arrivals or buffer accesses in the kernel must be made here too.
 """
 from __future__ import annotations
 
@@ -22,7 +28,7 @@ import pytest
 
 from synth import workloads as W
 
-RING, TILE, PAGE = 5, 128, 64
+SRING, VRING, TILE, PAGE = 13, 9, 128, 64
 
 
 class Bar:
@@ -31,6 +37,7 @@ class Bar:
 
     def arrive(self):
         self.pending -= 1
+        assert self.pending >= 0, f"{self.name}: too many arrivals"
         if self.pending == 0:
             self.done += 1
             self.pending = self.count
@@ -44,17 +51,17 @@ class Bar:
         return ok
 
 
-class Ring:
-    def __init__(self):
-        self.s = self.n = 0
+class RingPos:
+    def __init__(self, R: int):
+        self.R, self.s, self.n = R, 0, 0
+
+    @property
+    def ph(self):
+        return (self.n // self.R) & 1
 
     def next(self):
         self.n += 1
-        self.s = (self.s + 1) % RING
-
-    def skip(self, m: int):
-        for _ in range(m):
-            self.next()
+        self.s = (self.s + 1) % self.R
 
 
 def ntiles(p0, p1):
@@ -90,117 +97,278 @@ def split_segments(seq_lens, T, t, G):
     return out
 
 
-def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True,
-                 seg_guard: bool = True):
+class Hazard(AssertionError):
+    pass
+
+
+def expect(cond, what):
+    if not cond:
+        raise Hazard(what)
+
+
+def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str = "",
+                    slow: str = ""):
     """Returns None when every role finishes, else the blocked roles.
-    `guard` = False drops the value-MMA role's wait for S(x+1), `seg_guard`
-    = False the score-MMA role's wait for the previous segment's last PV.
-    Issued copies complete in random order (a separate copy-engine role)."""
+
+    pair: the four-CTA form (sides L = leader, P = peer on both the score
+    and the value side); else the two-CTA form (side L only).  rescale: the
+    correction warps rescale O at every tile after the first.  drop names a
+    wait to leave out (planted mistakes): "s_free", "pvd_land", "q_empty",
+    "pvd_rescale", "zdone".  slow: roles whose names start with it
+    run only when nothing else can (a slow role widens the windows in which
+    the others race ahead)."""
     rnd = random.Random(seed)
-    pending = []
-    full = [Bar(f"full{i}") for i in range(RING)]
-    empty = [Bar(f"empty{i}") for i in range(RING)]
-    s_full = [Bar("s_full0"), Bar("s_full1")]
-    p_full = [Bar("p_full0"), Bar("p_full1")]
-    pv_done = [Bar("pv_done0"), Bar("pv_done1")]
-    q_full, q_empty, o_free = Bar("q_full"), Bar("q_empty"), Bar("o_free")
+    sides = "LP" if pair else "L"
+    nside = len(sides)
+    pending = []            # copies issued, not yet landed: (callback)
+    nst_s = 5 if pair else 9
+    # ---- barriers (one object per CTA where each CTA has its own)
+    full_s = [Bar(f"full_s{i}", 1) for i in range(SRING)]          # leader's
+    empty_s = {x: [Bar(f"empty_s{x}{i}") for i in range(SRING)] for x in sides}
+    s_full = {x: [Bar(f"s_full{x}0"), Bar(f"s_full{x}1")] for x in sides}
+    s_free = [Bar("s_free0", nside), Bar("s_free1", nside)]        # leader's
+    q_ready = Bar("q_ready", nside)
+    qr = {x: Bar(f"qr{x}") for x in sides}
+    q_empty = {x: Bar(f"q_empty{x}") for x in sides}
+    pvd_s = {x: [Bar(f"pvd_s{x}0"), Bar(f"pvd_s{x}1")] for x in sides}
+    full_v = [Bar(f"full_v{i}", 1) for i in range(VRING)]          # leader's
+    empty_v = {x: [Bar(f"empty_v{x}{i}") for i in range(VRING)] for x in sides}
+    land = {x: [Bar(f"land{x}0"), Bar(f"land{x}1")] for x in sides}
+    o_ok = [Bar("o_ok0", nside), Bar("o_ok1", nside)]              # leader's
+    pvd_v = {x: [Bar(f"pvd_v{x}0"), Bar(f"pvd_v{x}1")] for x in sides}
+    zb, zdone = Bar("zb"), Bar("zdone")
+    # ---- buffer contents
+    ring_s = {x: [None] * SRING for x in sides}     # stage number held
+    ring_v = {x: [None] * VRING for x in sides}
+    sbuf = {x: [None, None] for x in sides}         # tile whose S is held
+    landing = {x: [None, None] for x in sides}      # tile whose P is held
+    landing_read = {x: [None, None] for x in sides}  # last tile whose P the PV consumed
+    qc = {x: None for x in sides}                   # segment whose q~ is in TMEM
+    qr_data = {x: None for x in sides}              # segment whose RoPE block landed
+    o_state = {x: {"seg": None, "last": None, "read": None} for x in sides}
 
-    def producer():
-        rp, k = Ring(), 0
-        for _, p0, p1 in segs:
+    seg_list = [(i, s) for i, s in enumerate(segs) if ntiles(s[1], s[2]) > 0]
+
+    # -------------------------------------------------------------- score side
+    def producer_s(x):
+        rp = RingPos(SRING)
+        for k, (_, (_, p0, p1)) in enumerate(seg_list):
             n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            if k > 0:
-                yield q_empty, k - 1
-            q_full.arrive()
-            for i in range(n + 1):
-                nsc = 9 if i < n else 0
-                nv = nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0
-                for _ in range(nsc + nv):
-                    if rp.n >= RING:
-                        yield empty[rp.s], rp.n // RING - 1
-                    pending.append(full[rp.s])
+            if k > 0 and "q_empty" not in drop:
+                yield q_empty[x], k - 1
+
+            def land_qr(x=x, k=k):
+                qr_data[x] = k
+                qr[x].arrive()
+            pending.append(land_qr)
+            for _ in range(n):
+                for _ in range(nst_s):
+                    if rp.n >= SRING:
+                        yield empty_s[x][rp.s], rp.n // SRING - 1
+                    stage, slot = rp.n, rp.s
+
+                    def land_s(x=x, slot=slot, stage=stage):
+                        ring_s[x][slot] = stage
+                        if not pair:
+                            full_s[slot].arrive()
+                        else:
+                            land_pair_s[slot].append(x)
+                            if len(land_pair_s[slot]) == 2:
+                                land_pair_s[slot].clear()
+                                full_s[slot].arrive()
+                    pending.append(land_s)
                     rp.next()
-            k += 1
 
-    def score_mma():
-        rp, g, k = Ring(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            yield q_full, k
-            for i in range(n + 1):
-                if i < n:
-                    gs = g + i
-                    if gs >= 2:
-                        yield pv_done[gs & 1], (gs - 2) >> 1
-                    if i == 0 and k > 0 and seg_guard:
-                        yield pv_done[(gs - 1) & 1], (gs - 1) >> 1
-                    for _ in range(9):
-                        yield full[rp.s], rp.n // RING
-                        empty[rp.s].arrive()
-                        rp.next()
-                    s_full[gs & 1].arrive()
-                    if i == n - 1:
-                        q_empty.arrive()
-                if i >= 1:
-                    rp.skip(nslabs(p0 + (i - 1) * TILE, p1))
-            g += n
-            k += 1
+    land_pair_s = [[] for _ in range(SRING)]   # pair: both halves complete the leader's barrier
 
-    def value_mma():
-        rp, g, k = Ring(), 0, 0
-        for _, p0, p1 in segs:
+    def issuer_s():
+        rp, g = RingPos(SRING), 0
+        for k, (_, (_, p0, p1)) in enumerate(seg_list):
             n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            for i in range(n + 1):
-                if i < n:
-                    rp.skip(9)
-                if i >= 1:
-                    gv = g + i - 1
-                    if i == 1 and k > 0:
-                        yield o_free, k - 1
-                    yield p_full[gv & 1], gv >> 1
-                    if guard and i < n:
-                        yield s_full[(gv + 1) & 1], (gv + 1) >> 1
-                    for _ in range(nslabs(p0 + (i - 1) * TILE, p1)):
-                        yield full[rp.s], rp.n // RING
-                        empty[rp.s].arrive()
-                        rp.next()
-                    pv_done[gv & 1].arrive()
-            g += n
-            k += 1
-
-    def softmax():
-        g = 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
+            yield q_ready, k
             for i in range(n):
-                yield s_full[g & 1], g >> 1
-                if i > 0 and rescale:
-                    yield pv_done[(g - 1) & 1], (g - 1) >> 1
-                p_full[g & 1].arrive()
-                g += 1
-            yield pv_done[(g - 1) & 1], (g - 1) >> 1
-            o_free.arrive()
+                gs = g + i
+                if gs >= 2 and "s_free" not in drop:
+                    yield s_free[gs & 1], (gs - 2) >> 1
+                for _ in range(nst_s):
+                    yield full_s[rp.s], rp.n // SRING
+                    for x in sides:
+                        expect(ring_s[x][rp.s] == rp.n, f"score slot {rp.s} of {x} holds "
+                               f"{ring_s[x][rp.s]}, MMA wants stage {rp.n}")
+                        expect(qc[x] == k, f"q~ of {x} holds segment {qc[x]}, S wants {k}")
+                        expect(qr_data[x] == k, f"RoPE block of {x} holds {qr_data[x]}, want {k}")
+                    for x in sides:
+                        empty_s[x][rp.s].arrive()
+                    rp.next()
+                for x in sides:
+                    expect(sbuf[x][gs & 1] is None or sbuf[x][gs & 1] == "read",
+                           f"S buffer {gs & 1} of {x} overwritten before it was read")
+                    sbuf[x][gs & 1] = gs
+                    s_full[x][gs & 1].arrive()
+                if i == n - 1:
+                    for x in sides:
+                        q_empty[x].arrive()
+            g += n
 
-    roles = {"score": score_mma(), "value": value_mma(), "softmax": softmax(),
-             "producer": producer()}
+    def softmax(x):
+        g = 0
+        for k, (_, (_, p0, p1)) in enumerate(seg_list):
+            n = ntiles(p0, p1)
+            if k > 0 and "q_empty" not in drop:
+                yield q_empty[x], k - 1
+            yield qr[x], k
+            qc[x] = k
+            q_ready.arrive()
+            for i in range(n):
+                yield s_full[x][g & 1], g >> 1
+                expect(sbuf[x][g & 1] == g, f"softmax {x} wants S({g}), buffer holds "
+                       f"{sbuf[x][g & 1]}")
+                sbuf[x][g & 1] = "read"
+                s_free[g & 1].arrive()
+                if g >= 2 and "pvd_land" not in drop:
+                    yield pvd_s[x][g & 1], (g - 2) >> 1
+                expect(landing[x][g & 1] is None or landing_read[x][g & 1] == landing[x][g & 1],
+                       f"landing {g & 1} of {x} rewritten before PV read P({landing[x][g & 1]})")
+                landing[x][g & 1] = g
+                land[x][g & 1].arrive()
+                g += 1
+
+    # -------------------------------------------------------------- value side
+    def partial(ts, v, p1):
+        return p1 - (ts + 32 * v) < 32
+
+    land_pair_v = [[] for _ in range(VRING)]
+
+    def producer_v(x):
+        rp, nz = RingPos(VRING), 0
+        for _, (_, p0, p1) in seg_list:
+            n = ntiles(p0, p1)
+            for i in range(n):
+                ts = p0 + i * TILE
+                for v in range(nslabs(ts, p1)):
+                    for _ in range(1 if pair else 2):
+                        if rp.n >= VRING:
+                            yield empty_v[x][rp.s], rp.n // VRING - 1
+                        part = pair and x == "P" and partial(ts, v, p1)
+                        if part and nz > 0 and "zdone" not in drop:
+                            yield zdone, nz - 1
+                        stage, slot = rp.n, rp.s
+
+                        def land_v(x=x, slot=slot, stage=stage, part=part):
+                            ring_v[x][slot] = stage
+                            if part:
+                                zb.arrive()
+                            elif pair:
+                                land_pair_v[slot].append(x)
+                                if len(land_pair_v[slot]) == 2:
+                                    land_pair_v[slot].clear()
+                                    full_v[slot].arrive()
+                            else:
+                                full_v[slot].arrive()
+                        pending.append(land_v)
+                        if part:
+                            nz += 1
+                        rp.next()
+
+    def relay():
+        rp, nz = RingPos(VRING), 0
+        for _, (_, p0, p1) in seg_list:
+            n = ntiles(p0, p1)
+            for i in range(n):
+                ts = p0 + i * TILE
+                for v in range(nslabs(ts, p1)):
+                    if partial(ts, v, p1):
+                        yield zb, nz
+                        expect(ring_v["P"][rp.s] == rp.n, "relay zeroes the wrong stage")
+                        land_pair_v[rp.s].append("P")
+                        if len(land_pair_v[rp.s]) == 2:
+                            land_pair_v[rp.s].clear()
+                            full_v[rp.s].arrive()
+                        zdone.arrive()
+                        nz += 1
+                    rp.next()
+
+    def issuer_v():
+        rp, g = RingPos(VRING), 0
+        for k, (_, (_, p0, p1)) in enumerate(seg_list):
+            n = ntiles(p0, p1)
+            for i in range(n):
+                gv = g + i
+                # o_ok of a segment's first tile comes from the correction
+                # warps after their read-out of the previous segment's O
+                yield o_ok[gv & 1], gv >> 1
+                for x in sides:
+                    expect(landing[x][gv & 1] == gv, f"PV({gv}) reads landing of {x} holding "
+                           f"P({landing[x][gv & 1]})")
+                    st = o_state[x]
+                    if i == 0:
+                        expect(k == 0 or st["read"] == k - 1,
+                               f"O of {x} reset for segment {k} before segment {k - 1} was read")
+                        st["seg"], st["last"] = k, None
+                    else:
+                        expect(st["last"] == gv - 1, f"PV({gv}) on O of {x} after PV({st['last']})")
+                    expect(st.get("rescaled_for", gv) == gv,
+                           f"O of {x} rescaled for tile {st.get('rescaled_for')} before PV({gv})")
+                for _ in range(nslabs(p0 + i * TILE, p1)):
+                    for _ in range(1 if pair else 2):
+                        yield full_v[rp.s], rp.n // VRING
+                        for x in sides:
+                            expect(ring_v[x][rp.s] == rp.n, f"value slot {rp.s} of {x} holds "
+                                   f"{ring_v[x][rp.s]}, MMA wants stage {rp.n}")
+                        for x in sides:
+                            empty_v[x][rp.s].arrive()
+                        rp.next()
+                for x in sides:
+                    landing_read[x][gv & 1] = gv
+                    o_state[x]["last"] = gv
+                    o_state[x].pop("rescaled_for", None)
+                    pvd_v[x][gv & 1].arrive()
+                    pvd_s[x][gv & 1].arrive()
+            g += n
+
+    def correction(x):
+        g = 0
+        for k, (_, (_, p0, p1)) in enumerate(seg_list):
+            n = ntiles(p0, p1)
+            for i in range(n):
+                yield land[x][g & 1], g >> 1
+                expect(landing[x][g & 1] == g, f"correction {x} reads f, l of "
+                       f"P({landing[x][g & 1]}) for tile {g}")
+                if rescale and i > 0:
+                    if "pvd_rescale" not in drop:
+                        yield pvd_v[x][(g - 1) & 1], (g - 1) >> 1
+                    st = o_state[x]
+                    expect(st["seg"] == k and st["last"] == g - 1,
+                           f"rescale of O of {x} for tile {g} after PV({st['last']})")
+                    st["rescaled_for"] = g
+                o_ok[g & 1].arrive()
+                g += 1
+            yield pvd_v[x][(g - 1) & 1], (g - 1) >> 1
+            st = o_state[x]
+            expect(st["seg"] == k and st["last"] == g - 1,
+                   f"epilogue of {x} reads O after PV({st['last']}), segment ends at {g - 1}")
+            st["read"] = k
+
+    roles = {"issuer_s": issuer_s(), "issuer_v": issuer_v()}
+    for x in sides:
+        roles[f"producer_s{x}"] = producer_s(x)
+        roles[f"softmax{x}"] = softmax(x)
+        roles[f"producer_v{x}"] = producer_v(x)
+        roles[f"correction{x}"] = correction(x)
+    if pair:
+        roles["relay"] = relay()
     waiting = {r: None for r in roles}
     alive = list(roles)
     while alive:
         cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
-        if pending and (not cand or rnd.random() < 0.5):
-            pending.pop(rnd.randrange(len(pending))).arrive()
+        if pending and (not cand or rnd.random() < 0.4):
+            pending.pop(rnd.randrange(len(pending)))()
             continue
         if not cand:
             return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
-        r = rnd.choice(cand) if seed is not None else cand[0]
+        fast = [r for r in cand if not (slow and r.startswith(slow))]
+        pick = fast if fast and rnd.random() < 0.97 else cand
+        r = rnd.choice(pick) if seed is not None else pick[0]
         try:
             waiting[r] = next(roles[r])
         except StopIteration:
@@ -209,469 +377,70 @@ def run_protocol(segs, rescale: bool, seed: int | None, guard: bool = True,
     return None
 
 
-@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 8])
-def test_single_and_multi_segment(n_tiles):
-    segs = [(0, 0, n_tiles * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200)]
-    for seed in range(12):
-        assert run_protocol(segs, seed % 2 == 0, seed) is None
+SEGS = [(0, 0, 5 * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200),
+        (5, 0, 2 * TILE), (6, 0, TILE), (7, 0, 100), (8, 0, 33), (9, 0, 31)]
+
+
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 8, 13])
+def test_single_and_multi_segment(pair, n_tiles):
+    segs = [(0, 0, n_tiles * TILE)] + SEGS[1:]
+    for seed in range(10):
+        assert run_sv_protocol(segs, pair, seed % 2 == 0, seed) is None
 
 
 @pytest.mark.parametrize("name", ["b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2"])
 def test_workload_split_plans(name):
     wl = W.config(name)
+    pair = wl.T % 2 == 0
     G = 148 // (2 * wl.T)
-    for t in range(wl.T):
-        plans = split_segments(wl.seq_lens, wl.T, t, G)
-        for c, segs in enumerate(plans):
-            if name == "b128-l16k-t2" and c % 4:
-                continue   # long splits: every fourth keeps the test short
-            for rescale, seed in ((False, None), (True, 7), (False, 11)):
-                assert run_protocol(segs, rescale, seed) is None, (t, c)
+    t = wl.T - 1 if pair else 0   # a pair iterates its odd token's range
+    plans = split_segments(wl.seq_lens, wl.T, t, G)
+    for c, segs in enumerate(plans):
+        if c % 5:
+            continue   # every fifth split keeps the test short
+        for rescale, seed in ((False, None), (True, 7)):
+            assert run_sv_protocol(segs, pair, rescale, seed) is None, (name, c)
 
 
-def test_model_catches_segment_start_aliasing():
-    """Without the score-MMA role's wait for the previous segment's last PV,
-    a one-tile segment followed by another lets that role pass a parity wait
-    on a slot whose value-stage fill of the lap before has not landed."""
-    segs = [(0, 0, TILE), (1, 0, 3 * TILE - 40)]
+# the role that falls behind when a wait is missing, for each planted mistake
+SLOW_FOR = {"s_free": "softmax", "pvd_land": "issuer_v", "q_empty": "issuer_s",
+            "pvd_rescale": "issuer_v"}
+
+
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("drop", list(SLOW_FOR))
+def test_model_catches_dropped_waits(pair, drop):
+    """Leaving out any one of these waits lets some interleaving read or
+    overwrite a buffer at the wrong time: the checks above are not vacuous."""
     failures = 0
     for seed in range(40):
         try:
-            failures += run_protocol(segs, seed % 2 == 0, seed, seg_guard=False) is not None
+            failures += run_sv_protocol(SEGS, pair, True, seed, drop=drop,
+                                        slow=SLOW_FOR[drop]) is not None
         except AssertionError:
             failures += 1
     assert failures > 0
 
 
-def test_model_catches_lap_aliasing():
-    """Without its wait on S(x+1) the value-MMA role can pass a parity wait
-    on a slot one lap behind: some interleaving of a 3-tile segment shows it,
-    so the checks above are not vacuous."""
-    failures = 0
-    for seed in range(20):
-        try:
-            failures += run_protocol([(0, 0, 3 * TILE)], False, seed, guard=False) is not None
-        except AssertionError:
-            failures += 1
-    assert failures > 0
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("slow", ["softmax", "issuer_v", "issuer_s", "correction", "producer"])
+def test_slow_roles(pair, slow):
+    """The full protocol under the same adversarial schedules."""
+    for seed in range(8):
+        assert run_sv_protocol(SEGS, pair, seed % 2 == 0, seed, slow=slow) is None
 
 
-# ---------------------------------------------------------------------------
-# Paired kernel (even T): a cluster of two CTAs, one per query token, shares
-# every cache tile.  The even CTA issues all MMAs with cta_group::2; each CTA
-# loads its half of each stage into its own 10-slot ring, and both halves
-# complete the even CTA's `ready` barrier (modelled as one arrival per CTA).
-# A value slab past the visible end is the exception: the odd CTA loads it
-# against a local barrier and its relay warp completes it on `ready` after
-# zeroing stale rows; the relay also forwards the odd CTA's query image.
-# Commits reach both CTAs (multicast); the softmax warps of both CTAs arrive
-# on the even CTA's p_full and o_free.  Ring step i of a segment holds score
-# blocks 0-4 of tile i, the value slabs of tile i-1, then score blocks 5-8 of
-# tile i, so PV(i-1) overlaps S(i).
-
-PRING = 10
-
-
-def step_items(i, n, nv_prev):
-    """('S', b) / ('V', v) items of ring step i (i = 0..n) in ring order."""
-    nsc = 9 if i < n else 0
-    head = 5 if nsc else 0
-    out = [("S", b) for b in range(head)]
-    out += [("V", v) for v in range(nv_prev if i >= 1 else 0)]
-    out += [("S", b) for b in range(head, nsc)]
-    return out
-
-
-class Ring10(Ring):
-    def next(self):
-        self.n += 1
-        self.s = (self.s + 1) % PRING
-
-
-def run_pair_protocol(segs, rescale: bool, seed: int | None, seg_guard: bool = True):
-    """seg_guard: the score role waits for PV of the previous tile before the
-    first tile of a later segment."""
-    rnd = random.Random(seed)
-    ready = [Bar(f"ready{i}", 2) for i in range(PRING)]
-    zb = Bar("zb")
-    empty = {r: [Bar(f"empty{r}{i}") for i in range(PRING)] for r in "LP"}
-    s_full = {r: [Bar(f"s_full{r}0"), Bar(f"s_full{r}1")] for r in "LP"}
-    pv_done = {r: [Bar(f"pv_done{r}0"), Bar(f"pv_done{r}1")] for r in "LP"}
-    q_empty = {r: Bar(f"q_empty{r}") for r in "LP"}
-    p_full = [Bar("p_full0", 2), Bar("p_full1", 2)]
-    q_ready, q_full_p, o_free = Bar("q_ready", 2), Bar("q_fullP"), Bar("o_free", 2)
-
-    def steps(n, p0, p1):
-        for i in range(n + 1):
-            yield i, step_items(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
-
-    def partial(i, item, p0, p1):
-        kind, v = item
-        return kind == "V" and p1 - (p0 + (i - 1) * TILE + 32 * v) < 32
-
-    def producer(side):
-        rp, k = Ring10(), 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            if k > 0:
-                yield q_empty[side], k - 1
-            (q_ready if side == "L" else q_full_p).arrive()
-            for i, items in steps(n, p0, p1):
-                for item in items:
-                    if rp.n >= PRING:
-                        yield empty[side][rp.s], rp.n // PRING - 1
-                    if side == "P" and partial(i, item, p0, p1):
-                        zb.arrive()
-                    else:
-                        ready[rp.s].arrive()
-                    rp.next()
-            k += 1
-
-    def relay():
-        rp, k, nz = Ring10(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            yield q_full_p, k
-            q_ready.arrive()
-            for i, items in steps(n, p0, p1):
-                for item in items:
-                    if partial(i, item, p0, p1):
-                        yield zb, nz
-                        ready[rp.s].arrive()
-                        nz += 1
-                    rp.next()
-            k += 1
-
-    def both(bars):
-        for b in bars:
-            b.arrive()
-
-    def score_mma():
-        rp, g, k = Ring10(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            yield q_ready, k
-            for i, items in steps(n, p0, p1):
-                gs = g + i
-                if i < n:
-                    if gs >= 2:
-                        yield pv_done["L"][gs & 1], (gs - 2) >> 1
-                    if seg_guard and i == 0 and gs >= 1:
-                        yield pv_done["L"][(gs - 1) & 1], (gs - 1) >> 1
-                for kind, _ in items:
-                    if kind == "S":
-                        yield ready[rp.s], rp.n // PRING
-                        both([empty["L"][rp.s], empty["P"][rp.s]])
-                    rp.next()
-                if i < n:
-                    both([s_full["L"][gs & 1], s_full["P"][gs & 1]])
-                    if i == n - 1:
-                        both([q_empty["L"], q_empty["P"]])
-            g += n
-            k += 1
-
-    def value_mma():
-        rp, g, k = Ring10(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            for i, items in steps(n, p0, p1):
-                gv = g + i - 1
-                if i >= 1:
-                    if i == 1 and k > 0:
-                        yield o_free, k - 1
-                    yield p_full[gv & 1], gv >> 1
-                for kind, _ in items:
-                    if kind == "V":
-                        yield ready[rp.s], rp.n // PRING
-                        both([empty["L"][rp.s], empty["P"][rp.s]])
-                    rp.next()
-                if i >= 1:
-                    both([pv_done["L"][gv & 1], pv_done["P"][gv & 1]])
-            g += n
-            k += 1
-
-    def softmax(side):
-        g = 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            for i in range(n):
-                yield s_full[side][g & 1], g >> 1
-                if i > 0 and rescale:
-                    yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
-                p_full[g & 1].arrive()
-                g += 1
-            yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
-            o_free.arrive()
-
-    roles = {"producerL": producer("L"), "producerP": producer("P"), "relay": relay(),
-             "score": score_mma(), "value": value_mma(), "softmaxL": softmax("L"),
-             "softmaxP": softmax("P")}
-    waiting = {r: None for r in roles}
-    alive = list(roles)
-    while alive:
-        cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
-        if not cand:
-            return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
-        r = rnd.choice(cand) if seed is not None else cand[0]
-        try:
-            waiting[r] = next(roles[r])
-        except StopIteration:
-            alive.remove(r)
-            waiting[r] = None
-    return None
-
-
-@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 8, 13])
-def test_pair_single_and_multi_segment(n_tiles):
-    segs = [(0, 0, n_tiles * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200),
-            (5, 0, 2 * TILE), (6, 0, TILE)]
-    for seed in range(16):
-        assert run_pair_protocol(segs, seed % 2 == 0, seed) is None
-
-
-def test_pair_workload_split_plan():
-    for name in ("b128-l16k-t2", "b64-paged"):
-        wl = W.config(name)
-        G = 148 // 4
-        plans = split_segments(wl.seq_lens, 2, 1, G)
-        for c, segs in enumerate(plans):
-            if c % 3:
-                continue
-            for rescale, seed in ((False, None), (True, 5)):
-                assert run_pair_protocol(segs, rescale, seed) is None, (name, c)
-
-
-# Paired kernel, 16 KB stages: a stage carries two score blocks (or the last
-# one) or two value slabs (or the last one) of this CTA's half, in a 5-slot
-# ring.  Ring step i: score stages {0,1}, {2,3}, the value stages of tile
-# i-1, then score stages {4,5}, {6,7}, {8}.
-
-PRING2 = 5
-
-
-def step_items2(i, n, nv_prev):
-    """('S', first block) / ('V', first slab) stages of ring step i."""
-    score = [("S", b) for b in (0, 2, 4, 6, 8)] if i < n else []
-    vals = [("V", v) for v in range(0, nv_prev, 2)] if i >= 1 else []
-    return score[:2] + vals + score[2:] if score else vals
-
-
-class Ring5(Ring):
-    pass
-
-
-def run_pair16_protocol(segs, rescale: bool, seed: int | None, items_fn=None,
-                        slabs_per_stage: int = 2, in_order: bool = False):
-    """items_fn / slabs_per_stage: the step layout (default: two slabs per
-    value stage, step_items2).  Issued copies complete in random order (a
-    separate copy-engine role), unless in_order."""
-    items_fn = items_fn or step_items2
-    rnd = random.Random(seed)
-    pending = []   # barriers of issued, not yet completed copies
-    R = PRING2
-    ready = [Bar(f"ready{i}", 2) for i in range(R)]
-    zb = Bar("zb")
-    empty = {r: [Bar(f"empty{r}{i}") for i in range(R)] for r in "LP"}
-    s_full = {r: [Bar(f"s_full{r}0"), Bar(f"s_full{r}1")] for r in "LP"}
-    pv_done = {r: [Bar(f"pv_done{r}0"), Bar(f"pv_done{r}1")] for r in "LP"}
-    q_empty = {r: Bar(f"q_empty{r}") for r in "LP"}
-    p_full = [Bar("p_full0", 2), Bar("p_full1", 2)]
-    q_ready, q_full_p, o_free = Bar("q_ready", 2), Bar("q_fullP"), Bar("o_free", 2)
-
-    def steps(n, p0, p1):
-        for i in range(n + 1):
-            yield i, items_fn(i, n, nslabs(p0 + (i - 1) * TILE, p1) if i >= 1 else 0)
-
-    def partial(i, item, p0, p1):
-        kind, v = item
-        if kind != "V":
-            return False
-        last = min(v + slabs_per_stage, nslabs(p0 + (i - 1) * TILE, p1)) - 1
-        return p1 - (p0 + (i - 1) * TILE + 32 * last) < 32
-
-    def producer(side):
-        rp, k = Ring(), 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            if k > 0:
-                yield q_empty[side], k - 1
-            (q_ready if side == "L" else q_full_p).arrive()
-            for i, items in steps(n, p0, p1):
-                for item in items:
-                    if rp.n >= R:
-                        yield empty[side][rp.s], rp.n // R - 1
-                    if side == "P" and partial(i, item, p0, p1):
-                        pending.append(zb)
-                    else:
-                        pending.append(ready[rp.s])
-                    if in_order:
-                        pending.pop(0).arrive()
-                    rp.next()
-            k += 1
-
-    def copy_engine():
-        while True:
-            if pending:
-                pending.pop(rnd.randrange(len(pending))).arrive()
-            yield None
-
-    def relay():
-        rp, k, nz = Ring(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            yield q_full_p, k
-            q_ready.arrive()
-            for i, items in steps(n, p0, p1):
-                for item in items:
-                    if partial(i, item, p0, p1):
-                        yield zb, nz
-                        ready[rp.s].arrive()
-                        nz += 1
-                    rp.next()
-            k += 1
-
-    def both(bars):
-        for b in bars:
-            b.arrive()
-
-    def score_mma():
-        rp, g, k = Ring(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            yield q_ready, k
-            for i, items in steps(n, p0, p1):
-                gs = g + i
-                if i < n:
-                    if gs >= 2:
-                        yield pv_done["L"][gs & 1], (gs - 2) >> 1
-                    if i == 0 and gs >= 1:
-                        yield pv_done["L"][(gs - 1) & 1], (gs - 1) >> 1
-                for kind, _ in items:
-                    if kind == "S":
-                        yield ready[rp.s], rp.n // R
-                        both([empty["L"][rp.s], empty["P"][rp.s]])
-                    rp.next()
-                if i < n:
-                    both([s_full["L"][gs & 1], s_full["P"][gs & 1]])
-                    if i == n - 1:
-                        both([q_empty["L"], q_empty["P"]])
-            g += n
-            k += 1
-
-    def value_mma():
-        rp, g, k = Ring(), 0, 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            for i, items in steps(n, p0, p1):
-                gv = g + i - 1
-                if i >= 1:
-                    if i == 1 and k > 0:
-                        yield o_free, k - 1
-                    yield p_full[gv & 1], gv >> 1
-                for kind, _ in items:
-                    if kind == "V":
-                        yield ready[rp.s], rp.n // R
-                        both([empty["L"][rp.s], empty["P"][rp.s]])
-                    rp.next()
-                if i >= 1:
-                    both([pv_done["L"][gv & 1], pv_done["P"][gv & 1]])
-            g += n
-            k += 1
-
-    def softmax(side):
-        g = 0
-        for _, p0, p1 in segs:
-            n = ntiles(p0, p1)
-            if n == 0:
-                continue
-            for i in range(n):
-                yield s_full[side][g & 1], g >> 1
-                if i > 0 and rescale:
-                    yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
-                p_full[g & 1].arrive()
-                g += 1
-            yield pv_done[side][(g - 1) & 1], (g - 1) >> 1
-            o_free.arrive()
-
-    roles = {"producerL": producer("L"), "producerP": producer("P"), "relay": relay(),
-             "score": score_mma(), "value": value_mma(), "softmaxL": softmax("L"),
-             "softmaxP": softmax("P")}
-    engine = copy_engine()
-    waiting = {r: None for r in roles}
-    alive = list(roles)
-    while alive:
-        cand = [r for r in alive if waiting[r] is None or waiting[r][0].ready(waiting[r][1])]
-        if pending and (not cand or rnd.random() < 0.5):
-            next(engine)
-            continue
-        if not cand:
-            return {r: (waiting[r][0].name, waiting[r][1]) for r in alive}
-        r = rnd.choice(cand) if seed is not None else cand[0]
-        try:
-            waiting[r] = next(roles[r])
-        except StopIteration:
-            alive.remove(r)
-            waiting[r] = None
-    return None
-
-
-@pytest.mark.parametrize("n_tiles", [1, 2, 3, 5, 8, 13])
-def test_pair16_single_and_multi_segment(n_tiles):
-    segs = [(0, 0, n_tiles * TILE), (1, 0, 3 * TILE - 40), (2, 0, 64), (3, 0, 0), (4, 64, 200),
-            (5, 0, 2 * TILE), (6, 0, TILE), (7, 0, 100)]
-    for seed in range(16):
-        assert run_pair16_protocol(segs, seed % 2 == 0, seed) is None
-
-
-def test_pair16_workload_split_plan():
-    for name in ("b128-l16k-t2", "b64-paged"):
-        wl = W.config(name)
-        plans = split_segments(wl.seq_lens, 2, 1, 148 // 4)
-        for c, segs in enumerate(plans):
-            if c % 3:
-                continue
-            for rescale, seed in ((False, None), (True, 5)):
-                assert run_pair16_protocol(segs, rescale, seed) is None, (name, c)
-
-
-# A ring order that is unsafe when copies complete out of order: value slabs
-# all between score stages {2,3} and {4,5} with one slab per stage.  The
-# last slab's slot was last used by this step's first score stage, which
-# the value role's waits do not cover.
-
-def step_items_unsafe(i, n, nv_prev):
-    score = [("S", b) for b in (0, 2, 4, 6, 8)] if i < n else []
-    vals = [("V", v) for v in range(nv_prev)] if i >= 1 else []
-    return score[:2] + vals + score[2:] if score else vals
-
-
-def test_model_catches_out_of_order_hazard():
-    """With step_items_unsafe a slow copy lets the value role pass a parity
-    wait a lap early: the model, whose copies complete in random order,
-    reports it."""
+def test_model_catches_dropped_relay_wait():
+    """Without the producer's wait for the relay, two partial value slabs of
+    one-tile segments can both land on the local barrier before the relay
+    waits: a parity wait passes a phase late."""
+    segs = [(b, 0, 20 + b) for b in range(8)]
     failures = 0
     for seed in range(60):
         try:
-            failures += run_pair16_protocol([(0, 0, 6 * TILE)], False, seed,
-                                            step_items_unsafe, 1) is not None
+            failures += run_sv_protocol(segs, True, False, seed, drop="zdone",
+                                        slow="relay") is not None
         except AssertionError:
             failures += 1
     assert failures > 0

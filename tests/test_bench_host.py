@@ -110,3 +110,17 @@ def test_work_model_matches_closed_forms():
     k2, _, _, _ = bench.work_model(W.config("b128-l16k-t2"))
     vis = sum(2 * S - 1 for S in W.config("b128-l16k-t2").seq_lens)
     assert k2["attend"][1] == 2 * vis * 128 * (576 + 512)
+
+
+def test_work_model_query_path():
+    """With the query path the step reads W^DQ [1536, 5120], W^UQ [16384,
+    1536] and W^QR [8192, 5120] instead of taking the queries as input."""
+    from synth import workloads as W
+    wl = W.config("b1-l4096")
+    _, b0, f0, _ = bench.work_model(wl)
+    k, b1, f1, _ = bench.work_model(wl, query_path=True)
+    assert k["query_down"][1] == 2 * 1536 * 5120
+    assert k["query_up"][1] == 2 * 16384 * 1536
+    assert k["query_rope"][1] == 2 * 8192 * 5120
+    assert b1 - b0 == (1536 * 5120 + 16384 * 1536 + 8192 * 5120) * 2 - 128 * 192 * 2
+    assert f1 - f0 == 2 * (1536 * 5120 + 16384 * 1536 + 8192 * 5120)
