@@ -89,3 +89,21 @@ def query(dims, h_row, w):
     q_c = _matvec(w["w_uq"], c_q)
     q_r = _matvec(w["w_qr"], h_row)
     return [q_c[i * dn:(i + 1) * dn] + q_r[i * dr:(i + 1) * dr] for i in range(H)]
+
+
+def decode_layers(dims, layers, h_new, T):
+    """Scalar decode through a stack of layers: h_{j+1} = h_j + u_j.
+
+    layers[j]: {"w": matrices as row lists, "prefix_h": hidden rows of the
+    cached positions of layer j}; h_new: T rows of layer 0's new hidden
+    states.  Each layer's cache is its prefix rows followed by the rows of
+    its own input; its queries come from its own input.
+    """
+    h = [list(r) for r in h_new]
+    for layer in layers:
+        w = layer["w"]
+        seq = [list(r) for r in layer["prefix_h"]] + h
+        q = [query(dims, r, w) for r in h]
+        u = decode(dims, seq, q, w, T)
+        h = [[a + b for a, b in zip(hr, ur)] for hr, ur in zip(h, u)]
+    return h

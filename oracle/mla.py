@@ -214,6 +214,40 @@ def decode_absorbed(dims, rows: np.ndarray, q: np.ndarray, w: dict, T: int) -> d
     return {"u": u, "o": o, "o_lat": o_lat}
 
 
+def decode_layers(dims, layers: list, h_new: np.ndarray, T: int, base: float | None = None,
+                  form: str = "explicit") -> dict:
+    """A decode step through a stack of MLA attention layers.
+
+    The pages count the cache over all l layers of the model ([V2-arch] ch.2
+    §2: (d_c + d_h^R) x l elements per token); each layer has its own weights
+    and its own cache.  Reading (the pages give no block structure beyond
+    attention and the MoE FFN, which is out of scope, and no normalisation):
+    layer j + 1 takes h_{j+1} = h_j + u_j, the residual connection of a
+    transformer block around the attention output.  ``layers[j]`` holds
+    "w" (the eight matrices of ``query_from_hidden`` and the decode) and
+    "prefix_rows" (layer j's cached rows of positions 0..S-T-1).  ``h_new``
+    [T, d] are layer 0's hidden states of the T new tokens at positions
+    S-T..S-1.  Each layer appends the rows of its own input h_j, makes the
+    queries of its own input and decodes them.  Returns h_L [T, d] and the
+    per-layer outputs u [L, T, d].
+    """
+    base = dims.rope_base if base is None else base
+    h = np.asarray(h_new, dtype=np.float64)
+    us = []
+    for layer in layers:
+        w = layer["w"]
+        prefix = np.asarray(layer["prefix_rows"], dtype=np.float64)
+        S = prefix.shape[0] + T
+        new_rows = latent_rows(h, w["w_dkv"], w["w_kr"], np.arange(S - T, S), base)
+        rows = np.concatenate([prefix, new_rows])
+        q = query_from_hidden(dims, h, w["w_dq"], w["w_uq"], w["w_qr"])
+        fn = decode_explicit if form == "explicit" else decode_absorbed
+        u = fn(dims, rows, q, w, T)["u"]
+        us.append(u)
+        h = h + u
+    return {"h": h, "u": np.stack(us)}
+
+
 def attention_weights_absorbed(dims, rows, q, w, T, t, head) -> np.ndarray:
     """Softmax weights of one (query token, head) in the absorbed form."""
     dc, dn = dims.d_latent, dims.d_nope

@@ -449,3 +449,93 @@ def test_planted_query_swapped_parts(monkeypatch):
         return np.concatenate([q[..., dims.d_nope:], q[..., :dims.d_nope]], axis=2)[..., :q.shape[2]]
     monkeypatch.setattr(mla, "query_from_hidden", bad)
     assert not _query_pins_pass()
+
+
+# --------------------------------------------------------------------------
+# multi-layer step: h_{j+1} = h_j + u_j, each layer with its own cache
+# --------------------------------------------------------------------------
+def _stack_case():
+    case = _load("layer_stack_examples.json")["cases"][0]
+    layers = []
+    for L in case["layers"]:
+        w = {k: np.array(L[k], dtype=np.float64) for k in QW}
+        rows = _rows(WORKED_DIMS, w, np.array(L["prefix_h"]))
+        layers.append({"w": w, "prefix_rows": rows})
+    return case, layers
+
+
+@pytest.mark.parametrize("form", ["explicit", "absorbed"])
+def test_layer_stack_worked_example(form):
+    case, layers = _stack_case()
+    r = mla.decode_layers(WORKED_DIMS, layers, np.array(case["h_new"]), 1, form=form)
+    np.testing.assert_allclose(r["u"], case["expect_u"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(r["h"], case["expect_h"], rtol=0, atol=1e-14)
+
+
+def test_layer_stack_worked_example_brute():
+    case = _load("layer_stack_examples.json")["cases"][0]
+    layers = [{"w": {k: L[k] for k in QW}, "prefix_h": L["prefix_h"]} for L in case["layers"]]
+    h = brute.decode_layers(WORKED_DIMS, layers, case["h_new"], 1)
+    np.testing.assert_allclose(h, case["expect_h"], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_layer_stack_brute_force_agrees(T):
+    d = dataclasses.replace(SMALL_SHAPES[1], d_cq=3)
+    rng = np.random.default_rng(11 + T)
+    layers, blayers = [], []
+    for _ in range(3):
+        w = {"w_dkv": rng.standard_normal((d.d_latent, d.d_model)),
+             "w_kr": rng.standard_normal((d.d_rope, d.d_model)),
+             "w_uk": rng.standard_normal((d.n_heads * d.d_nope, d.d_latent)),
+             "w_uv": rng.standard_normal((d.n_heads * d.d_v, d.d_latent)),
+             "w_o": rng.standard_normal((d.d_model, d.n_heads * d.d_v)) * 0.3,
+             "w_dq": rng.standard_normal((3, d.d_model)),
+             "w_uq": rng.standard_normal((d.n_heads * d.d_nope, 3)),
+             "w_qr": rng.standard_normal((d.n_heads * d.d_rope, d.d_model))}
+        ph = rng.standard_normal((4, d.d_model))
+        layers.append({"w": w, "prefix_rows": _rows(d, w, ph)})
+        blayers.append({"w": {k: v.tolist() for k, v in w.items()}, "prefix_h": ph.tolist()})
+    h0 = rng.standard_normal((T, d.d_model))
+    r = mla.decode_layers(d, layers, h0, T)
+    hb = brute.decode_layers(d, blayers, h0.tolist(), T)
+    assert _rel(r["h"], np.array(hb)) < 1e-12
+
+
+def _stack_pins_pass():
+    try:
+        test_layer_stack_worked_example("explicit")
+        test_layer_stack_brute_force_agrees(2)
+    except AssertionError:
+        return False
+    return True
+
+
+def test_planted_stack_without_residual(monkeypatch):
+    orig = mla.decode_layers
+
+    def bad(dims, layers, h_new, T, base=None, form="explicit"):
+        h = np.asarray(h_new, dtype=np.float64)
+        us = []
+        for layer in layers:
+            r = orig(dims, [layer], h, T, base, form)
+            us.append(r["u"][0])
+            h = r["u"][0]          # the residual dropped
+        return {"h": h, "u": np.stack(us)}
+    monkeypatch.setattr(mla, "decode_layers", bad)
+    assert not _stack_pins_pass()
+
+
+def test_planted_stack_same_input_every_layer(monkeypatch):
+    orig = mla.decode_layers
+
+    def bad(dims, layers, h_new, T, base=None, form="explicit"):
+        h0 = np.asarray(h_new, dtype=np.float64)
+        h, us = h0, []
+        for layer in layers:
+            r = orig(dims, [layer], h0, T, base, form)   # every layer reads h_0
+            us.append(r["u"][0])
+            h = h + r["u"][0]
+        return {"h": h, "u": np.stack(us)}
+    monkeypatch.setattr(mla, "decode_layers", bad)
+    assert not _stack_pins_pass()
