@@ -36,7 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s and latent-cache GB/s (% of B300 roofline), 1 GPU"
-DEFAULT_STEPS = {"tiny-fp32": 200, "b1-l4096": 1000, "b64-paged": 300, "b4-l128k": 300, "b128-l16k-t2": 50}
+DEFAULT_STEPS = {"tiny-fp32": 200, "b1-l4096": 1000, "b64-paged": 300, "b4-l128k": 300,
+                 "b128-l16k-t2": 50, "b1-l4096-x60": 30, "b64-paged-x8": 30}
 
 
 # ----------------------------------------------------------------------------- setup
@@ -46,7 +47,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="b128-l16k-t2",
-                    choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2"])
+                    choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2",
+                             "b1-l4096-x60", "b64-paged-x8"])
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--query-path", action="store_true",
                     help="time the step from the hidden states alone (mla_layer_step: the "
@@ -58,6 +60,8 @@ def parse():
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.config]
     a.warmup = max(a.warmup, 3)
+    if a.config.endswith(("-x60", "-x8")):
+        a.query_path = True   # a layer stack makes every layer's queries from its input
     return a
 
 
@@ -136,6 +140,13 @@ def work_model(wl, query_path=False):
         tot_bytes += (cq * D + H * dn * cq + H * dr * D) * es - M * H * (dn + dr) * es
         steps += ["query_down", "query_rope", "query_up"]
     tot_flops = sum(k[n][1] for n in steps)
+    if wl.layers > 1:
+        # every layer reads its own weights and cache; the residual reads h and
+        # u and writes h; the queries and new rows of layers > 0 come from h
+        k["residual"] = (3 * M * D * es, 1.0 * M * D)
+        tot_bytes = (tot_bytes + k["residual"][0]) * wl.layers
+        tot_flops = (tot_flops + k["residual"][1]) * wl.layers
+        return k, tot_bytes, tot_flops, cache_rows * R * es * wl.layers
     return k, tot_bytes, tot_flops, cache_rows * R * es
 
 
@@ -208,7 +219,9 @@ def oracle_sample_setup(wl, device):
     import torch
     from oracle import case as ocase
     from oracle import mla as omla
-    w64 = ocase.weights_f64(wl, device=device)
+    names = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o") + \
+        (("w_dq", "w_uq", "w_qr") if wl.dims.d_cq and wl.layers > 1 else ())
+    w64 = ocase.weights_f64(wl, names=names, device=device)
     L = wl.lens[0]
     rows = np.empty((L, wl.dims.row_width))
     for p0 in range(0, L, 8192):
@@ -217,7 +230,10 @@ def oracle_sample_setup(wl, device):
         rows[p0:p1] = omla.latent_rows(h, w64["w_dkv"], w64["w_kr"], np.arange(p0, p1),
                                        wl.dims.rope_base)
     h_new = wl.h_rows(0, L, L + wl.T, device=device).to(torch.float64).cpu().numpy()
-    q64 = wl.q(device=device)[0].to(torch.float64).cpu().numpy()
+    if wl.layers > 1:   # layer 0 of the stack: queries from the query path
+        q64 = omla.query_from_hidden(wl.dims, h_new, w64["w_dq"], w64["w_uq"], w64["w_qr"])
+    else:
+        q64 = wl.q(device=device)[0].to(torch.float64).cpu().numpy()
     return {"w": w64, "rows": rows, "h_new": h_new, "q": q64}
 
 
@@ -244,7 +260,7 @@ def oracle_sample_step(wl, st, head):
 def time_oracle(wl, st, steps=None, seconds=None):
     """Returns (tokens/s, seconds timed, steps timed, sample description)."""
     H = wl.dims.n_heads
-    per_step_tokens = wl.T / H        # one head of one sequence's T tokens
+    per_step_tokens = wl.T / (H * wl.layers)   # one head of one layer of one sequence
     n, t0 = 0, time.perf_counter()
     while True:
         oracle_sample_step(wl, st, n % H)
@@ -254,9 +270,10 @@ def time_oracle(wl, st, steps=None, seconds=None):
             break
         if seconds is not None and el >= seconds:
             break
-    sample = (f"sequence 0 (cache {wl.lens[0]} + {wl.T} new tokens), one of {H} heads per step, "
-              f"explicit fp64 form incl. the new rows' W^DKV/W^KR; tokens/s = T/{H} per step "
-              f"/ step time")
+    lay = f" of layer 0 of {wl.layers}" if wl.layers > 1 else ""
+    sample = (f"sequence 0 (cache {wl.lens[0]} + {wl.T} new tokens), one of {H} heads{lay} per "
+              f"step, explicit fp64 form incl. the new rows' W^DKV/W^KR; tokens/s = "
+              f"T/({H}*{wl.layers}) per step / step time")
     return per_step_tokens * n / el, el, n, sample
 
 
@@ -319,8 +336,13 @@ def run_mla(a, wl, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
     props = torch.cuda.get_device_properties(dev)
-    st = DeviceState(wl, device=local_rank, query_path=a.query_path)
-    step = st.layer_step if a.query_path else st.step
+    if wl.layers > 1:
+        from mla_latent_kv_82_b300.workload import StackState
+        st = StackState(wl, device=local_rank)
+        step = st.step
+    else:
+        st = DeviceState(wl, device=local_rank, query_path=a.query_path)
+        step = st.layer_step if a.query_path else st.step
     torch.cuda.synchronize()
     l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
     # L2 flush: write a 2x-L2 buffer, then read another one, so the timed step
@@ -336,15 +358,19 @@ def run_mla(a, wl, rank, local_rank, world):
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
-    if st.mla.check_status() != 0:
+    check_status = st.check_status if wl.layers > 1 else st.mla.check_status
+    launch_count = (lambda: sum(m.launch_count() for m in st.mlas)) if wl.layers > 1 \
+        else st.mla.launch_count
+    prof_ctxs = [m.ctx for m in st.mlas] if wl.layers > 1 else [st.mla.ctx]
+    if check_status() != 0:
         raise RuntimeError("device status set during warm-up")
 
     # one decode step (append + decode) as a CUDA graph, replayed every step
-    n0 = st.mla.launch_count()
+    n0 = launch_count()
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         step()
-    launches_per_step = st.mla.launch_count() - n0
+    launches_per_step = launch_count() - n0
     for _ in range(a.warmup):
         flush()
         g_step.replay()
@@ -374,7 +400,7 @@ def run_mla(a, wl, rank, local_rank, world):
     if world > 1:
         dist.barrier()
     step_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs), dev)
-    status = st.mla.check_status()
+    status = check_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     time.sleep(0.2)
@@ -387,7 +413,8 @@ def run_mla(a, wl, rank, local_rank, world):
     # ---- per-kernel durations: the same steps with an event at every kernel
     # boundary (events keep kernels from overlapping, so this pass only
     # apportions time between kernels; the step time comes from the pass above)
-    m.mla_profile_enable(st.mla.ctx, 1)
+    for cx in prof_ctxs:
+        m.mla_profile_enable(cx, 1)
     g_prof = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_prof):
         step()
@@ -395,9 +422,11 @@ def run_mla(a, wl, rank, local_rank, world):
     for i in range(a.steps):
         flush()
         g_prof.replay()
-        for name, ms in m.mla_profile_read(st.mla.ctx):
-            kt.setdefault(name, []).append(ms)
-    m.mla_profile_enable(st.mla.ctx, 0)
+        for cx in prof_ctxs:
+            for name, ms in m.mla_profile_read(cx):
+                kt.setdefault(name, []).append(ms)
+    for cx in prof_ctxs:
+        m.mla_profile_enable(cx, 0)
 
     # ---- roofline of the dominant kernel and of the whole step
     kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path)
@@ -430,13 +459,15 @@ def run_mla(a, wl, rank, local_rank, world):
     if not a.no_e2e:
         # the step's inputs (new hidden states, queries, positions, lengths)
         # sit in one pinned staging buffer and go over in one copy
-        in_h = st.step_inputs.cpu().pin_memory()
-        out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        dev_in = st.h0 if wl.layers > 1 else st.step_inputs
+        dev_out = st.h if wl.layers > 1 else st.out
+        in_h = dev_in.cpu().pin_memory()
+        out_h = torch.empty(dev_out.shape, dtype=dev_out.dtype).pin_memory()
 
         def e2e_step():
-            st.step_inputs.copy_(in_h, non_blocking=True)
+            dev_in.copy_(in_h, non_blocking=True)
             step()
-            out_h.copy_(st.out, non_blocking=True)
+            out_h.copy_(dev_out, non_blocking=True)
 
         g_e2e = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_e2e):
@@ -475,12 +506,16 @@ def run_mla(a, wl, rank, local_rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic: seeded N(0,1) hidden states and queries, N(0,1/fan_in) weights",
-        "config": {"workload": wl.name + ("+query-path" if a.query_path else ""),
-                   "batch": wl.B, "T": wl.T,
+        "config": {"workload": wl.name + ("+query-path" if a.query_path and wl.layers == 1
+                                          else ""),
+                   "batch": wl.B, "T": wl.T, "layers": wl.layers,
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
                    f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
                    "step's event bracket)",
-                   "graph": ("each step is one CUDA-graph replay of mla_layer_step (queries "
+                   "graph": ("each step is one CUDA-graph replay of mla_multi_layer_step "
+                             f"through {wl.layers} layers (each: queries from its input, "
+                             "append, decode, residual)") if wl.layers > 1 else
+                            ("each step is one CUDA-graph replay of mla_layer_step (queries "
                              "from the new hidden states, append, decode)") if a.query_path else
                             ("each step is one CUDA-graph replay of mla_append_decode "
                              "(append the new rows, then decode them)"),

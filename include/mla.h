@@ -189,6 +189,32 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
                           int T, void* out, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* One decode step through a stack of n_layers attention layers, each with
+ * its own context (weights, d_cq > 0) and its own cache pool; the pools
+ * share one page layout (block_table, num_pages).  The pages count the cache
+ * over all l layers of the model (liang.world ch.2 §2: (d_c + d_h^R) x l
+ * elements per token).  Layer j runs mla_layer_step on h_j (its new rows go
+ * into caches[j], its queries come from h_j) and then
+ *   h_{j+1} = h_j + u_j
+ * (fp32 addition, rounded to the context dtype): the residual connection of
+ * a transformer block around the attention output; the FFN sublayer and any
+ * normalisation are outside this library.
+ *   h          device, [batch*T, d_model], in/out: h_0 on entry, h_L on
+ *              return (overwritten layer by layer).
+ *   caches     host array of n_layers device pool pointers.
+ *   u_scratch  device, [batch*T, d_model]: holds u of the last layer.
+ *   workspace  as for mla_layer_step, shared by the layers (one at a time).
+ * Other arguments as for mla_layer_step.  All contexts must share dtype,
+ * d_model and device; a bad argument of any layer is reported before
+ * anything is enqueued. */
+mla_status mla_multi_layer_step(mla_ctx* const* ctxs, int n_layers, void* h,
+                                const int32_t* positions, void* const* caches,
+                                int num_pages, const int32_t* block_table,
+                                int max_pages, const int32_t* seq_lens,
+                                int batch, int T, void* u_scratch,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream);
+
 /* Decode without a workspace argument, for callers that cannot allocate
  * device memory when they decode (a fixed memory budget reserved up front,
  * an allocator that is not reachable from the issuing thread, a plugin that

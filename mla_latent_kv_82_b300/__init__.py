@@ -30,6 +30,7 @@ EXPORTED = (
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
     "mla_decode_static_workspace", "mla_append_decode", "mla_layer_step",
+    "mla_multi_layer_step",
 )
 
 
@@ -80,6 +81,8 @@ def _load() -> ctypes.CDLL:
         "mla_append_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp],
                               i32),
         "mla_layer_step": ([vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp], i32),
+        "mla_multi_layer_step": ([ctypes.POINTER(vp), i32, vp, vp, ctypes.POINTER(vp), i32, vp,
+                                  i32, vp, i32, i32, vp, vp, sz, vp], i32),
         "mla_profile_read": ([vp, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_char_p), i32], i32),
     }
@@ -142,6 +145,17 @@ def mla_layer_step(ctx, h, positions, cache, num_pages, block_table, max_pages, 
                    T, out, workspace, workspace_bytes, stream) -> int:
     return _lib.mla_layer_step(ctx, h, positions, cache, num_pages, block_table, max_pages,
                                seq_lens, batch, T, out, workspace, workspace_bytes, stream)
+
+
+def mla_multi_layer_step(ctxs, h, positions, caches, num_pages, block_table, max_pages, seq_lens,
+                         batch, T, u_scratch, workspace, workspace_bytes, stream) -> int:
+    """ctxs and caches: sequences of context handles and pool pointers, one per layer."""
+    n = len(ctxs)
+    c_arr = (ctypes.c_void_p * n)(*ctxs)
+    k_arr = (ctypes.c_void_p * n)(*caches)
+    return _lib.mla_multi_layer_step(c_arr, n, h, positions, k_arr, num_pages, block_table,
+                                     max_pages, seq_lens, batch, T, u_scratch, workspace,
+                                     workspace_bytes, stream)
 
 
 def mla_decode_static_workspace(ctx, q, cache, num_pages, block_table, max_pages, seq_lens,

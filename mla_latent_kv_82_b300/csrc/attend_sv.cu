@@ -14,11 +14,13 @@
 //
 //   score CTA   TMEM: q~ (the 512 latent features of Q, bf16 packed two per
 //               column, 256 columns) and two S buffers (2 x 128 columns);
-//               shared memory: the RoPE block of Q (16 KB) and a 13-stage
-//               ring of score blocks [tokens x 64 features].
-//               S = q~ C_lat^T (A from TMEM) + RoPE(q^R) k^R^T (A from
-//               shared memory); softmax from registers; P (bf16) and the
-//               row statistics stored into the value CTA's landing buffer.
+//               shared memory: the RoPE block of Q (16 KB), a staging
+//               buffer for P and an 11-stage ring of score blocks [tokens x
+//               64 features].  S = q~ C_lat^T (A from TMEM) + RoPE(q^R)
+//               k^R^T (A from shared memory); softmax from registers; P
+//               (bf16) and the row statistics staged in local shared memory
+//               and pushed by one bulk copy into the value CTA's landing
+//               buffer (its bytes complete the landing barrier there).
 //   value CTA   TMEM: O (512 columns); shared memory: two landing buffers
 //               (P [128 heads x 128 tokens] + rescale factor + running row
 //               sum) and a 9-stage ring of value slabs [32 tokens x 256
@@ -49,20 +51,33 @@ namespace {
 using namespace att;
 
 constexpr uint32_t kStage = 16384;
-constexpr int kSRing = 13;                                  // score ring stages
 constexpr int kVRing = 9;                                   // value ring stages
 // landing buffer: P [2 token blocks][128 heads][128 B] (SW128, K-major),
 // then the rescale factor f[128] and the running row sum l[128]
 constexpr uint32_t kLandP = 32768;
 constexpr uint32_t kLandBytes = kLandP + 512 + 512;         // 33792
 constexpr uint32_t kOffQr = 0;                              // score: RoPE block of Q
-constexpr uint32_t kOffSRing = 16384;
+constexpr uint32_t kOffStage = 16384;                       // score: P staging buffers
 constexpr uint32_t kOffLand = 0;                            // value: landing buffers
 constexpr uint32_t kOffVRing = 2 * kLandBytes;              // 67584
-constexpr uint32_t kOffBar = kOffSRing + kSRing * kStage;   // 229376, same in every CTA
-static_assert(kOffVRing + kVRing * kStage <= kOffBar, "value ring overlaps the barriers");
+
+// The score side's shared memory holds one staging buffer for P and an
+// 11-stage ring for a single query token (9 stages per tile), two staging
+// buffers and an 8-stage ring for a token pair (5 stages per tile).  With one
+// buffer a tile's P waits for the previous tile's copy to land; measured,
+// that wait bounds the pair kernel, while the single-token kernel is bound
+// by its score-block loads and gains from the deeper ring.
+template <bool kPair> struct SvLayout {
+  static constexpr int kStaging = kPair ? 2 : 1;
+  static constexpr int kSRing = kPair ? 8 : 11;
+  static constexpr uint32_t kOffSRing = kOffStage + kStaging * kLandBytes;
+  static constexpr uint32_t kOffBar = kOffSRing + kSRing * kStage;   // same in every CTA
+  static constexpr uint32_t kSmem = kOffBar + 512 + 1024;
+  static_assert(kOffVRing + kVRing * kStage <= kOffBar, "value ring overlaps the barriers");
+  static_assert(kOffSRing % 1024 == 0, "SW128 operands need 1 KB alignment");
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
 static_assert(kOffVRing % 1024 == 0 && kLandBytes % 1024 == 0, "SW128 operands need 1 KB alignment");
-constexpr uint32_t kSmemSV = kOffBar + 512 + 1024;
 
 // Barrier slots (8 bytes each) at kOffBar, at the same offset in every CTA of
 // a cluster so that multicast commits and remote arrivals can name them.
@@ -73,7 +88,7 @@ enum : int {
   kBSFree = 34,    // [2] score: S of that parity read by the softmax warps
   kBPvd = 36,      // [2] PV of tiles of that parity done (value: O may be read /
                    //     rescaled; score: that landing buffer may be rewritten)
-  kBLand = 38,     // [2] value: P of that parity landed (4 softmax warps)
+  kBLand = 38,     // [2] value: P of that parity landed (bulk copy from the score CTA)
   kBOok = 40,      // [2] value: O corrected for that tile (pair leader: 8 warps)
   kBQReady = 42,   // score: q~ stored in TMEM and the RoPE block landed
   kBQr = 43,       // score: RoPE block of Q landed (local copy)
@@ -81,6 +96,7 @@ enum : int {
   kBDrained = 46,  // this CTA's MMAs all complete
   kBZb = 47,       // odd value CTA: partial value slab landed locally
   kBZDone = 48,    // odd value CTA: relay finished a partial slab
+  kBStgFree = 49,  // score: the staged P of the last tile has landed (value CTA)
   kBSlot = 50      // TMEM base address (u32) and abort flag (u32)
 };
 
@@ -92,18 +108,59 @@ __device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, int* statu
   return warp_wait<kPair>(bar, parity, status, where);
 }
 
+// The four K steps (4 x 16 features) of one 64-feature score block: A from
+// TMEM at aq (8 columns per step), B the block's descriptor (32 bytes per
+// step); the first step accumulates if acc0.
+template <bool kPair>
+__device__ __forceinline__ void score_mma4(uint32_t d, uint32_t aq, uint64_t b, uint32_t idesc,
+                                           uint32_t acc0) {
+  if (kPair) {
+    tc::mma2_ts(d, aq, b, idesc, acc0);
+    tc::mma2_ts(d, aq + 8, b + 2, idesc, 1u);
+    tc::mma2_ts(d, aq + 16, b + 4, idesc, 1u);
+    tc::mma2_ts(d, aq + 24, b + 6, idesc, 1u);
+  } else {
+    tc::mma_ts(d, aq, b, idesc, acc0);
+    tc::mma_ts(d, aq + 8, b + 2, idesc, 1u);
+    tc::mma_ts(d, aq + 16, b + 4, idesc, 1u);
+    tc::mma_ts(d, aq + 24, b + 6, idesc, 1u);
+  }
+}
+
+// The same for the RoPE block with A (the rotated q^R) in shared memory.
+template <bool kPair>
+__device__ __forceinline__ void score_mma4_ss(uint32_t d, uint64_t a, uint64_t b,
+                                              uint32_t idesc) {
+  if (kPair) {
+    tc::mma2_ss(d, a, b, idesc, 1u);
+    tc::mma2_ss(d, a + 2, b + 2, idesc, 1u);
+    tc::mma2_ss(d, a + 4, b + 4, idesc, 1u);
+    tc::mma2_ss(d, a + 6, b + 6, idesc, 1u);
+  } else {
+    tc::mma_ss(d, a, b, idesc, 1u);
+    tc::mma_ss(d, a + 2, b + 2, idesc, 1u);
+    tc::mma_ss(d, a + 4, b + 4, idesc, 1u);
+    tc::mma_ss(d, a + 6, b + 6, idesc, 1u);
+  }
+}
+
 template <bool kPair>
 __global__ void __launch_bounds__(224, 1)
 attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 64}
                  const __grid_constant__ CUtensorMap tmS2,   // pool blocks, box {64, 64, 2}
                  const __grid_constant__ CUtensorMap tmV,    // pool blocks, box {64, 32, kPair ? 2 : 4}
                  const AttArgs a) {
+  using Lay = SvLayout<kPair>;
+  constexpr int kSRing = Lay::kSRing;
+  constexpr uint32_t kOffSRing = Lay::kOffSRing;
+  constexpr uint32_t kOffBar = Lay::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kBSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* sm_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);   // softmax warps
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = tc::cluster_rank();
@@ -136,7 +193,7 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       mbar_init(&bar[kBSFull + i], 1);
       mbar_init(&bar[kBSFree + i], pw);
       mbar_init(&bar[kBPvd + i], 1);
-      mbar_init(&bar[kBLand + i], 4);
+      mbar_init(&bar[kBLand + i], 1);
       mbar_init(&bar[kBOok + i], pw);
     }
     mbar_init(&bar[kBQReady], pw);
@@ -145,7 +202,9 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
     mbar_init(&bar[kBDrained], 1);
     mbar_init(&bar[kBZb], 1);
     mbar_init(&bar[kBZDone], 1);
+    mbar_init(&bar[kBStgFree], 1);
     *abort_flag = 0;
+    *sm_fail = 0;
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -291,23 +350,19 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
           if (!cwait<kPair>(&bar[kBFull + s], rp.ph, a.status, 75)) { ok = false; break; }
           tc::fence_after_sync();
           if (el) {
-            const int b0 = kPair ? 2 * j : j;
-            const int cnt = kPair ? (j == 4 ? 1 : 2) : 1;
-            for (int u = 0; u < cnt; ++u) {
-              const int b = b0 + u;
-              const uint64_t dRs = dR + ((s * kStage + u * 8192) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc = (b > 0 || kk > 0) ? 1u : 0u;
-                if (b < 8) {
-                  const uint32_t aq = tmem + kColQ + b * 32 + kk * 8;
-                  if (kPair) tc::mma2_ts(dcol, aq, dRs + kk * 2, idS, acc);
-                  else tc::mma_ts(dcol, aq, dRs + kk * 2, idS, acc);
-                } else {
-                  if (kPair) tc::mma2_ss(dcol, dQr + kk * 2, dRs + kk * 2, idS, acc);
-                  else tc::mma_ss(dcol, dQr + kk * 2, dRs + kk * 2, idS, acc);
-                }
-              }
+            // Each stage's MMAs are issued as straight-line code: a branch
+            // between two tcgen05.mma instructions was measured to slow their
+            // issue from 64 to about 95 cycles each (M = 128, N = 128).
+            const uint64_t dRs = dR + ((s * kStage) >> 4);
+            if (j < kNst - 1) {
+              // latent blocks: A = q~ from TMEM, 8 columns per K step of 16
+              const int b0 = kPair ? 2 * j : j;
+              const uint32_t aq = tmem + kColQ + b0 * 32;
+              score_mma4<kPair>(dcol, aq, dRs, idS, j > 0 ? 1u : 0u);
+              if (kPair) score_mma4<kPair>(dcol, aq + 32, dRs + (8192 >> 4), idS, 1u);
+            } else {
+              // RoPE block: A from shared memory
+              score_mma4_ss<kPair>(dcol, dQr, dRs, idS);
             }
             if (kPair) tc::mma2_commit_mc(smem_u32(&bar[kBEmpty + s]), (uint16_t)pair_mask);
             else tc::mma_commit(smem_u32(&bar[kBEmpty + s]));
@@ -340,6 +395,10 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
     // the log2 domain with a lazy rescale (m moves only when the maximum
     // grows by more than 2^kRescale, so P <= 256), P as bf16 into the value
     // CTA's landing buffer with the rescale factor f and the running sum l.
+    // The four warps meet at a named barrier twice per tile (the staging
+    // buffer is shared), so every decision to stop is taken by all of them
+    // together: a warp whose wait fails raises sm_fail and goes on to the
+    // next barrier; right after it every thread reads sm_fail and all stop.
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -349,7 +408,7 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
     SegIter it;
     it.init(&a, c, t_iter);
     int sb, p0, p1, slot, g = 0, k = 0;
-    bool ok = true;
+    bool ok = true, fail = false;
     while (ok && it.next(&sb, &p0, &p1, &slot)) {
       const int n = ntiles_of(p0, p1);
       const size_t prow = ((size_t)slot * a.T + t) * kHeads + row;
@@ -358,11 +417,10 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
         continue;
       }
       // ---- q~ of this segment's token: image blocks 0-7, row `row`
-      if (k > 0 && !cwait<kPair>(&bar[kBQEmpty], (k - 1) & 1, a.status, 76)) { ok = false; break; }
-      if (!warp_wait<false>(&bar[kBQr], k & 1, a.status, 77)) { ok = false; break; }
-      if (aborted()) { ok = false; break; }
-      tc::fence_after_sync();
-      {
+      if (!fail && k > 0) fail = !cwait<kPair>(&bar[kBQEmpty], (k - 1) & 1, a.status, 76);
+      if (!fail) fail = !warp_wait<false>(&bar[kBQr], k & 1, a.status, 77);
+      if (!fail) {
+        tc::fence_after_sync();
         const uint8_t* img = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes + prow_off;
 #pragma unroll 1
         for (int fb = 0; fb < 8; ++fb) {
@@ -377,69 +435,85 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
           }
           tc::tmem_st32(trow + kColQ + fb * 32, w);
         }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        if (kPair) tc::mbar_arrive_cluster_relaxed(cbar(kBQReady, lead_rank));
-        else tc::mbar_arrive(smem_u32(&bar[kBQReady]));
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair) tc::mbar_arrive_cluster_relaxed(cbar(kBQReady, lead_rank));
+          else tc::mbar_arrive(smem_u32(&bar[kBQReady]));
+        }
       }
       ++k;
       // ---- tiles
       const int p1_own = min(p1, a.lens[sb] - a.T + t + 1);   // this token's causal end
       float m_used = -INFINITY, l = 0.f;
       for (int i = 0; i < n; ++i, ++g) {
-        if (!cwait<kPair>(&bar[kBSFull + (g & 1)], (g >> 1) & 1, a.status, 78)) { ok = false; break; }
-        if (aborted()) { ok = false; break; }
-        tc::fence_after_sync();
-        uint32_t lo[64], hi[64];
-        const uint32_t scol = trow + kColS + (g & 1) * kTile;
-        tc::tmem_ld64(scol, lo);
-        tc::tmem_ld64(scol + 64, hi);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) {
-          if (kPair) tc::mbar_arrive_cluster_relaxed(cbar(kBSFree + (g & 1), lead_rank));
-          else tc::mbar_arrive(smem_u32(&bar[kBSFree + (g & 1)]));
-        }
-        const int valid = max(0, min(kTile, p1_own - (p0 + i * kTile)));
-        const float mx = (valid == kTile ? row_max<false>(lo, hi, valid)
-                                         : row_max<true>(lo, hi, valid)) * a.scale_log2;
-        float f = 1.f;
-        if (i == 0) {
-          m_used = mx;
-        } else if (mx > m_used + kRescale) {
-          f = exp2f(m_used - mx);
-          m_used = mx;
-          l *= f;
-        }
+        if (!fail) fail = !cwait<kPair>(&bar[kBSFull + (g & 1)], (g >> 1) & 1, a.status, 78);
         uint32_t pk[64];
-        const float psum = valid == kTile
-                               ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
-                               : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
-        l += psum;
-        // landing buffer g & 1 was last read by PV(g - 2)
-        if (g >= 2 && !bar_wait<true>(&bar[kBPvd + (g & 1)], ((g - 2) >> 1) & 1, a.status, 79)) {
-          ok = false;
+        float f = 1.f;
+        if (!fail) {
+          tc::fence_after_sync();
+          uint32_t lo[64], hi[64];
+          const uint32_t scol = trow + kColS + (g & 1) * kTile;
+          tc::tmem_ld64(scol, lo);
+          tc::tmem_ld64(scol + 64, hi);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if (kPair) tc::mbar_arrive_cluster_relaxed(cbar(kBSFree + (g & 1), lead_rank));
+            else tc::mbar_arrive(smem_u32(&bar[kBSFree + (g & 1)]));
+          }
+          const int valid = max(0, min(kTile, p1_own - (p0 + i * kTile)));
+          const float mx = (valid == kTile ? row_max<false>(lo, hi, valid)
+                                           : row_max<true>(lo, hi, valid)) * a.scale_log2;
+          if (i == 0) {
+            m_used = mx;
+          } else if (mx > m_used + kRescale) {
+            f = exp2f(m_used - mx);
+            m_used = mx;
+            l *= f;
+          }
+          const float psum = valid == kTile
+                                 ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
+                                 : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
+          l += psum;
+          // landing buffer g & 1 is free once PV(g - 2) has read it, and so
+          // is staging buffer g & 1 of a pair (its copy landed before that);
+          // the single staging buffer once the copy of P(g - 1) has landed
+          if (warp == 2) {
+            bool w = true;
+            if (!kPair && g >= 1)
+              w = bar_wait<true>(&bar[kBStgFree], (g - 1) & 1, a.status, 80);
+            if (w && g >= 2)
+              w = bar_wait<true>(&bar[kBPvd + (g & 1)], ((g - 2) >> 1) & 1, a.status, 79);
+            fail = !__all_sync(0xffffffffu, w);
+          }
         }
-        if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-        const uint32_t dst = land0 + (g & 1) * kLandBytes;
+        if (fail) *sm_fail = 1;
+        if (warp == 2 && lane == 0 && *abort_flag) *sm_fail = 1;
+        tc::named_sync(1, 128);
+        if (*sm_fail) { ok = false; break; }   // the same value for every thread
+        uint8_t* stg = smem + kOffStage + (kPair ? (g & 1) * kLandBytes : 0u);
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch) {
           const uint32_t off = (uint32_t)((ch >> 3) * 16384) + prow_off +
                                (uint32_t)(((ch & 7) ^ (row & 7)) << 4);
-          tc::st_cluster_v4(dst + off, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          *reinterpret_cast<uint4*>(stg + off) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
         }
-        tc::st_cluster_f32(dst + kLandP + row * 4, f);
-        tc::st_cluster_f32(dst + kLandP + 512 + row * 4, l);
-        tc::fence_proxy_async_cluster();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(cbar(kBLand + (g & 1), vrank));
+        reinterpret_cast<float*>(stg + kLandP)[row] = f;
+        reinterpret_cast<float*>(stg + kLandP + 512)[row] = l;
+        tc::fence_async_smem();   // the staged P is read by the bulk copy (async proxy)
+        tc::named_sync(1, 128);
+        if (warp == 2 && lane == 0) {
+          const uint32_t lb = cbar(kBLand + (g & 1), vrank);
+          tc::mbar_arrive_expect_tx_cluster(lb, kLandBytes);
+          tc::bulk_s2c(land0 + (g & 1) * kLandBytes, smem_u32(stg), kLandBytes, lb);
+        }
       }
       if (!ok) break;
       a.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
     }
-    if (!ok) set_abort();
+    if (!ok || fail) set_abort();
   } else if (!score && warp == 0) {
     // ------------------------------------------------------ value producer
     // Value slabs of every tile in order: single CTA, [32 tokens x 256
@@ -598,6 +672,7 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
     const int row = q4 * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const float* landf = reinterpret_cast<const float*>(smem + kOffLand + kLandP);
+    const uint32_t srank = rank - (kPair ? 2u : 1u);   // the score CTA of this token
     SegIter it;
     it.init(&a, c, t_iter);
     int sb, p0, p1, slot, g = 0;
@@ -615,6 +690,9 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       for (int i = 0; i < n; ++i, ++g) {
         if (!bar_wait<true>(&bar[kBLand + (g & 1)], (g >> 1) & 1, a.status, 86)) ok = false;
         if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
+        // the copy of P(g) has landed: the single staging buffer is free
+        if (!kPair && warp == 2 && lane == 0)
+          tc::mbar_arrive_cluster_relaxed(cbar(kBStgFree, srank));
         const float* lf = reinterpret_cast<const float*>(
             reinterpret_cast<const uint8_t*>(landf) + (g & 1) * kLandBytes);
         const float f = lf[row];
@@ -733,11 +811,11 @@ bool launch_sv(mla_ctx* ctx, const CUtensorMap& tmS, const CUtensorMap& tmS2,
                const CUtensorMap& tmV, const AttArgs& a, int G, int T, cudaStream_t st) {
   auto kern = attend_sv_kernel<kPair>;
   static std::atomic<uint64_t> attr_done{0};
-  if (smem_attr_once(attr_done, kern, (int)kSmemSV) != cudaSuccess) return false;
+  if (smem_attr_once(attr_done, kern, (int)SvLayout<kPair>::kSmem) != cudaSuccess) return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = kPair ? dim3(4, G, T / 2) : dim3(2 * G, T, 1);
   cfg.blockDim = dim3(224);
-  cfg.dynamicSmemBytes = kSmemSV;
+  cfg.dynamicSmemBytes = SvLayout<kPair>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -797,7 +875,7 @@ bool sv_setup(mla_ctx* ctx) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = pair ? dim3(4, 1, 1) : dim3(2, 1, 1);
     cfg.blockDim = dim3(224);
-    cfg.dynamicSmemBytes = kSmemSV;
+    cfg.dynamicSmemBytes = pair ? SvLayout<true>::kSmem : SvLayout<false>::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pair ? 4 : 2;
@@ -809,11 +887,11 @@ bool sv_setup(mla_ctx* ctx) {
     cudaError_t e;
     if (pair) {
       static std::atomic<uint64_t> done{0};
-      e = smem_attr_once(done, attend_sv_kernel<true>, (int)kSmemSV);
+      e = smem_attr_once(done, attend_sv_kernel<true>, (int)SvLayout<true>::kSmem);
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, attend_sv_kernel<true>, &cfg);
     } else {
       static std::atomic<uint64_t> done{0};
-      e = smem_attr_once(done, attend_sv_kernel<false>, (int)kSmemSV);
+      e = smem_attr_once(done, attend_sv_kernel<false>, (int)SvLayout<false>::kSmem);
       if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, attend_sv_kernel<false>, &cfg);
     }
     if (e != cudaSuccess) {

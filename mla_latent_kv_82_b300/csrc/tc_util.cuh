@@ -444,6 +444,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16, both ends 16-byte aligned) from this
+// CTA's shared memory to shared memory of a CTA of the cluster, counted on
+// an mbarrier of the destination CTA (cluster addresses from mapa_shared).
+__device__ __forceinline__ void bulk_s2c(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                         uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster and raise its expected
+// transaction count by `bytes` (no ordering of this thread's earlier writes).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster,
+                                                              uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+          bar_cluster),
+      "r"(bytes)
+      : "memory");
+}
+
 // 16-byte global load through the read-only path.
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 v;

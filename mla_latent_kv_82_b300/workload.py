@@ -116,3 +116,64 @@ class DeviceState:
         else:
             n, off, shape = B * T * d.n_heads * d.d_v, off_o, (B * T, d.n_heads * d.d_v)
         return self.ws[off:off + n * es].view(self.wl.torch_dtype).view(*shape)
+
+
+class StackState:
+    """A stack of wl.layers attention layers on one GPU: per-layer contexts
+    (with the query path), weights and cache pools sharing one block table,
+    each pool prefilled from that layer's own seeded hidden states.
+    ``step()`` runs mla_multi_layer_step on the new tokens' layer-0 hidden
+    states (copied into ``h`` first, so every step repeats the same work)."""
+
+    def __init__(self, wl, device: int = 0, chunk: int = 32768):
+        from . import MLA
+        self.wl = wl
+        self.dev = torch.device("cuda", device)
+        d, dt, T = wl.dims, wl.torch_dtype, wl.T
+        bt = wl.block_table()
+        self.bt = torch.as_tensor(bt, dtype=torch.int32, device=self.dev).contiguous()
+        self.num_pages = int(self.bt.max().item()) + 1
+        rows = self.num_pages * d.page_size
+        self.weights, self.mlas, self.caches = [], [], []
+        for j in range(wl.layers):
+            w = {n: wl.weight(n, device=self.dev, layer=j) for n in W_NAMES + Q_NAMES}
+            self.weights.append(w)
+            self.mlas.append(MLA(d, w, wl.dtype, max_position=max(wl.seq_lens), device=device))
+            self.caches.append(torch.empty((rows, d.row_width), dtype=dt, device=self.dev))
+        self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=self.dev)
+        self.pos_new = torch.tensor([L + t for L in wl.lens for t in range(T)],
+                                    dtype=torch.int32, device=self.dev)
+        self.h0 = torch.cat([wl.h_rows(b, L, L + T, device=self.dev)
+                             for b, L in enumerate(wl.lens)]).contiguous()
+        self.h = torch.empty_like(self.h0)
+        self.u = torch.empty_like(self.h0)
+        self.ws_bytes = self.mlas[0].workspace_size(wl.B, T, self.bt.shape[1])
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.dev)
+        for j in range(wl.layers):
+            for b, L in enumerate(wl.lens):
+                for p0 in range(0, L, chunk):
+                    p1 = min(L, p0 + chunk)
+                    h = wl.h_rows(b, p0, p1, device=self.dev, layer=j)
+                    pos = torch.arange(p0, p1, dtype=torch.int32, device=self.dev)
+                    self.mlas[j].compress_append(h, pos, self.bt[b:b + 1], self.caches[j], 1,
+                                                 p1 - p0)
+
+    def step(self, stream=None):
+        from . import MLAError, mla_multi_layer_step
+        s = stream if stream is not None else torch.cuda.current_stream()
+        self.h.copy_(self.h0)
+        st = mla_multi_layer_step([m.ctx for m in self.mlas], self.h.data_ptr(),
+                                  self.pos_new.data_ptr(), [c.data_ptr() for c in self.caches],
+                                  self.num_pages, self.bt.data_ptr(), self.bt.shape[1],
+                                  self.seq_lens.data_ptr(), self.wl.B, self.wl.T,
+                                  self.u.data_ptr(), self.ws.data_ptr(), self.ws_bytes,
+                                  s.cuda_stream)
+        if st != 0:
+            raise MLAError(st, "mla_multi_layer_step")
+
+    def check_status(self) -> int:
+        for m in self.mlas:
+            r = m.check_status()
+            if r:
+                return r
+        return 0

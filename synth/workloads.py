@@ -12,7 +12,8 @@ uses n_h = 4, d_c = 32, d_R = 8, d_h = 16, d = 64.
 
 Recipe (every value is seeded):
 * tensor ids: h=0, W^DKV=1, W^KR=2, W^UK=3, W^UV=4, W_O=5, q=6, and for the
-  query path W^DQ=7, W^UQ=8, W^QR=9;
+  query path W^DQ=7, W^UQ=8, W^QR=9; in a stack of layers, layer j's weights
+  and cached hidden states use id + 16 j (layer 0 the ids above);
 * h and q ~ N(0, 1); every weight ~ N(0, 1/fan_in), fan_in = input width;
 * sequence b has ``lens[b]`` cached tokens before the step and ``T`` new
   tokens; h of token p of sequence b is row ``b * row_stride + p`` of a
@@ -74,6 +75,7 @@ class Workload:
     T: int                # new (query) tokens per sequence
     shuffle_pages: bool
     seed: int = 0
+    layers: int = 1       # attention layers of a multi-layer step
 
     @property
     def B(self) -> int:
@@ -117,7 +119,7 @@ class Workload:
         return bt
 
     # ---- seeded tensors -------------------------------------------------
-    def weight(self, name: str, device="cpu") -> torch.Tensor:
+    def weight(self, name: str, device="cpu", layer: int = 0) -> torch.Tensor:
         d = self.dims
         spec = {
             "w_dkv": (TID_WDKV, (d.d_latent, d.d_model), d.d_model),
@@ -130,14 +132,16 @@ class Workload:
             "w_qr": (TID_WQR, (d.n_heads * d.d_rope, d.d_model), d.d_model),
         }[name]
         tid, shape, fan_in = spec
-        return gen.fill(self.seed, tid, shape, 1.0 / math.sqrt(fan_in),
+        return gen.fill(self.seed, tid + 16 * layer, shape, 1.0 / math.sqrt(fan_in),
                         self.torch_dtype, device=device)
 
-    def h_rows(self, b: int, p0: int, p1: int, device="cpu") -> torch.Tensor:
-        """Hidden states of tokens p0..p1-1 of sequence b, [p1-p0, d]."""
+    def h_rows(self, b: int, p0: int, p1: int, device="cpu", layer: int = 0) -> torch.Tensor:
+        """Hidden states of tokens p0..p1-1 of sequence b, [p1-p0, d] (layer j's
+        cached positions use their own seeded states; the new tokens' states of
+        layer j > 0 come from the layers below)."""
         d = self.dims.d_model
         start = (b * self.row_stride + p0) * d
-        return gen.fill(self.seed, TID_H, (p1 - p0, d), 1.0, self.torch_dtype,
+        return gen.fill(self.seed, TID_H + 16 * layer, (p1 - p0, d), 1.0, self.torch_dtype,
                         device=device, start=start)
 
     def q(self, device="cpu") -> torch.Tensor:
@@ -164,7 +168,13 @@ def config(name: str) -> Workload:
         return Workload("v2-b4-L131072", V2, "bf16", [131071] * 4, 1, False)
     if name == "b128-l16k-t2":   # batch 128, L=16384, two query tokens, full step
         return Workload("v2-b128-L16384-T2", V2, "bf16", [16384] * 128, 2, False)
+    if name == "b1-l4096-x60":   # the batch-1 step through 60 layers
+        return Workload("v2-b1-L4096-x60layers", V2, "bf16", [4095], 1, False, layers=60)
+    if name == "b64-paged-x8":   # the batch-64 paged step through 8 layers
+        return Workload("v2-b64-paged-Lrand-x8layers", V2, "bf16", paged_lens(), 1, True,
+                        layers=8)
     raise KeyError(name)
 
 
-CONFIG_NAMES = ("tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2")
+CONFIG_NAMES = ("tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2",
+                "b1-l4096-x60", "b64-paged-x8")

@@ -113,8 +113,8 @@ def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str
     pair: the four-CTA form (sides L = leader, P = peer on both the score
     and the value side); else the two-CTA form (side L only).  rescale: the
     correction warps rescale O at every tile after the first.  drop names a
-    wait to leave out (planted mistakes): "s_free", "pvd_land", "q_empty",
-    "pvd_rescale", "zdone".  slow: roles whose names start with it
+    wait to leave out (planted mistakes): "s_free", "pvd_land", "stg_free",
+    "q_empty", "pvd_rescale", "zdone".  slow: roles whose names start with it
     run only when nothing else can (a slow role widens the windows in which
     the others race ahead)."""
     rnd = random.Random(seed)
@@ -143,6 +143,9 @@ def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str
     sbuf = {x: [None, None] for x in sides}         # tile whose S is held
     landing = {x: [None, None] for x in sides}      # tile whose P is held
     landing_read = {x: [None, None] for x in sides}  # last tile whose P the PV consumed
+    staging = {x: [None, None] for x in sides}      # tile whose P each staging buffer holds
+    staging_sent = {x: [None, None] for x in sides}  # last tile whose staged P has landed
+    stg_free = {x: Bar(f"stg_free{x}") for x in sides}
     qc = {x: None for x in sides}                   # segment whose q~ is in TMEM
     qr_data = {x: None for x in sides}              # segment whose RoPE block landed
     o_state = {x: {"seg": None, "last": None, "read": None} for x in sides}
@@ -225,12 +228,32 @@ def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str
                        f"{sbuf[x][g & 1]}")
                 sbuf[x][g & 1] = "read"
                 s_free[g & 1].arrive()
+                # a single token stages P in one buffer, freed when the
+                # copy of P(g - 1) lands; a pair in two, buffer g & 1 freed
+                # with landing buffer g & 1 (PV(g - 2) done)
+                if not pair and g >= 1 and "stg_free" not in drop:
+                    yield stg_free[x], g - 1
                 if g >= 2 and "pvd_land" not in drop:
                     yield pvd_s[x][g & 1], (g - 2) >> 1
-                expect(landing[x][g & 1] is None or landing_read[x][g & 1] == landing[x][g & 1],
-                       f"landing {g & 1} of {x} rewritten before PV read P({landing[x][g & 1]})")
-                landing[x][g & 1] = g
-                land[x][g & 1].arrive()
+                sb = (g & 1) if pair else 0
+                # P(g) into the local staging buffer, then one bulk copy to
+                # the value CTA's landing buffer g & 1; the copy reads the
+                # staging buffer and lands some time later
+                expect(staging[x][sb] is None or staging_sent[x][sb] == staging[x][sb],
+                       f"staging of {x} rewritten before its copy of P({staging[x][sb]}) landed")
+                staging[x][sb] = g
+
+                def copy_lands(x=x, g=g, sb=sb):
+                    expect(staging[x][sb] == g, f"copy of P({g}) from {x} read a staging "
+                           f"buffer holding P({staging[x][sb]})")
+                    staging_sent[x][sb] = g
+                    expect(landing[x][g & 1] is None or
+                           landing_read[x][g & 1] == landing[x][g & 1],
+                           f"landing {g & 1} of {x} rewritten before PV read "
+                           f"P({landing[x][g & 1]})")
+                    landing[x][g & 1] = g
+                    land[x][g & 1].arrive()
+                pending.append(copy_lands)
                 g += 1
 
     # -------------------------------------------------------------- value side
@@ -334,6 +357,8 @@ def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str
                 yield land[x][g & 1], g >> 1
                 expect(landing[x][g & 1] == g, f"correction {x} reads f, l of "
                        f"P({landing[x][g & 1]}) for tile {g}")
+                if not pair:
+                    stg_free[x].arrive()
                 if rescale and i > 0:
                     if "pvd_rescale" not in drop:
                         yield pvd_v[x][(g - 1) & 1], (g - 1) >> 1
@@ -405,12 +430,14 @@ def test_workload_split_plans(name):
 
 # the role that falls behind when a wait is missing, for each planted mistake
 SLOW_FOR = {"s_free": "softmax", "pvd_land": "issuer_v", "q_empty": "issuer_s",
-            "pvd_rescale": "issuer_v"}
+            "pvd_rescale": "issuer_v", "stg_free": "correction"}
 
 
 @pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("drop", list(SLOW_FOR))
 def test_model_catches_dropped_waits(pair, drop):
+    if pair and drop == "stg_free":
+        pytest.skip("a pair stages P in two buffers and does not wait on stg_free")
     """Leaving out any one of these waits lets some interleaving read or
     overwrite a buffer at the wrong time: the checks above are not vacuous."""
     failures = 0

@@ -124,3 +124,17 @@ def test_work_model_query_path():
     assert k["query_rope"][1] == 2 * 8192 * 5120
     assert b1 - b0 == (1536 * 5120 + 16384 * 1536 + 8192 * 5120) * 2 - 128 * 192 * 2
     assert f1 - f0 == 2 * (1536 * 5120 + 16384 * 1536 + 8192 * 5120)
+
+
+def test_work_model_layer_stack():
+    """A stack reads every layer's weights and cache once per step, plus the
+    residual's h and u reads and h write."""
+    import dataclasses
+    from synth import workloads as W
+    one = dataclasses.replace(W.config("b1-l4096-x60"), layers=1)
+    _, b1, f1, c1 = bench.work_model(one, query_path=True)
+    k, b60, f60, c60 = bench.work_model(W.config("b1-l4096-x60"), query_path=True)
+    assert k["residual"] == (3 * 5120 * 2, 5120.0)
+    assert b60 == 60 * (b1 + 3 * 5120 * 2)
+    assert f60 == 60 * (f1 + 5120)
+    assert c60 == 60 * c1 == 60 * 4096 * 576 * 2
