@@ -28,6 +28,7 @@ struct AttArgs {
   const __nv_bfloat16* cache;
   float* part_o;
   float* part_lse;
+  __nv_bfloat16* o_lat;   // final latent output of sequences held by one split
   int* status;
   int B, T, max_pages, num_pages;
   float scale_log2;

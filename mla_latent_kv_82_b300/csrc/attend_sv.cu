@@ -422,18 +422,27 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       if (!fail) {
         tc::fence_after_sync();
         const uint8_t* img = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes + prow_off;
+        // two rounds of four feature blocks, 32 loads in flight per thread
 #pragma unroll 1
-        for (int fb = 0; fb < 8; ++fb) {
-          uint32_t w[32];
+        for (int f0 = 0; f0 < 8; f0 += 4) {
+          uint4 v[4][8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 v = tc::ld_nc_v4(img + fb * 16384 + ((j ^ (row & 7)) << 4));
-            w[4 * j] = v.x;
-            w[4 * j + 1] = v.y;
-            w[4 * j + 2] = v.z;
-            w[4 * j + 3] = v.w;
+          for (int fb = 0; fb < 4; ++fb)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[fb][j] = tc::ld_nc_v4(img + (f0 + fb) * 16384 + ((j ^ (row & 7)) << 4));
+#pragma unroll
+          for (int fb = 0; fb < 4; ++fb) {
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              w[4 * j] = v[fb][j].x;
+              w[4 * j + 1] = v[fb][j].y;
+              w[4 * j + 2] = v[fb][j].z;
+              w[4 * j + 3] = v[fb][j].w;
+            }
+            tc::tmem_st32(trow + kColQ + (f0 + fb) * 32, w);
           }
-          tc::tmem_st32(trow + kColQ + fb * 32, w);
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -725,13 +734,31 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       tc::fence_after_sync();
       // l = 0 only when this token sees none of the segment's tokens
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      for (int c0 = 0; c0 < kLat; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(trow + c0, v);
+      if (a.slot_base[sb + 1] - a.slot_base[sb] == 1) {
+        // the sequence lies in this split alone: O / l is its latent output
+        // (bf16, as the combine would write it); the combine skips it
+        __nv_bfloat16* od = a.o_lat + (((size_t)sb * a.T + t) * kHeads + row) * kLat;
+        for (int c0 = 0; c0 < kLat; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(trow + c0, v);
+          uint32_t w[8];
 #pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          __stcg(reinterpret_cast<float4*>(dst + c0 + j),
-                 make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
+          for (int j = 0; j < 8; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * j] * inv, v[2 * j + 1] * inv);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(od + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(od + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      } else {
+        for (int c0 = 0; c0 < kLat; c0 += 16) {
+          float v[16];
+          tc::tmem_ld16(trow + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            __stcg(reinterpret_cast<float4*>(dst + c0 + j),
+                   make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
+        }
       }
       tc::fence_before_sync();
     }
@@ -854,6 +881,7 @@ bool sv_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
   a.cache = cache;
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  a.o_lat = reinterpret_cast<__nv_bfloat16*>(ws + L.o_lat);
   a.status = ctx->status;
   a.B = B;
   a.T = T;

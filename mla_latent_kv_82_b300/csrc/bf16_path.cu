@@ -18,7 +18,8 @@ namespace {
 
 // Merge the split partials of one (token, head) into o_lat = sum_s w_s O_s /
 // sum_s w_s with w_s = 2^(lse_s - max lse): the log-sum-exp combine of
-// flash-decoding.  For sequences cut into many splits (a few long
+// flash-decoding.  A sequence held by one split alone is skipped: the
+// attention kernel wrote its o_lat directly.  For sequences cut into many splits (a few long
 // sequences), one CTA per (token, head): the split weights are formed
 // once in shared memory, then two groups of 128 threads (one float4 of the
 // 512 latent columns per thread) each sum every other split with eight
@@ -40,6 +41,7 @@ combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__
   const int b = m / T, t = m % T;
   const int s0 = slot_base[b];
   int n = slot_base[b + 1] - s0;
+  if (n == 1) return;   // one split held the whole sequence: it wrote o_lat itself
   if (n > kCombineMaxSlots) {   // cannot happen with the planner's slot counts
     if (threadIdx.x == 0) report(status, MLA_ERR_INVALID_ARG, 60);
     n = kCombineMaxSlots;
@@ -116,6 +118,7 @@ combine_rows_kernel(const float* __restrict__ part_o, const float* __restrict__ 
   const int m = mh / kHeads, head = mh % kHeads;
   const int b = m / T, t = m % T;
   const int s0 = slot_base[b], s1 = slot_base[b + 1];
+  if (s1 - s0 == 1) return;   // one split held the whole sequence: it wrote o_lat itself
   float lmax = -INFINITY;
   for (int s = s0; s < s1; ++s) lmax = fmaxf(lmax, part_lse[((size_t)s * T + t) * kHeads + head]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -24,9 +24,17 @@
 namespace mla {
 namespace {
 
-template <int NT> struct WgCfg {
-  static constexpr int kStages = NT == 16 ? 6 : NT == 32 ? 5 : NT == 64 ? 4 : NT == 128 ? 6 : 4;
-  static constexpr int kMinBlocks = NT <= 64 ? 2 : 1;
+// Token tiles up to 64 run two CTAs per SM.  The absorbed-query GEMM reads
+// K = 128 (two chunks), so two stages are all it can use, which also lets
+// two of its CTAs share an SM at any tile (measured: the append + absorbed
+// query launch at 256 tokens 72 -> 51 us).  Wide tiles of the long-K
+// projections keep one CTA per SM with a deep ring: halving the ring for two
+// CTAs per SM, with the extra K splits that brings, was measured slower
+// (W_O at 256 tokens 70 -> 82 us).
+template <int NT, int EPI = WG_ROWMAJOR> struct WgCfg {
+  static constexpr int kStages = EPI == WG_QIMG ? 2
+                               : NT == 16 ? 6 : NT == 32 ? 5 : NT == 64 ? 4 : NT == 128 ? 6 : 4;
+  static constexpr int kMinBlocks = (EPI == WG_QIMG || NT <= 64) ? 2 : 1;
   static constexpr uint32_t kA = 128 * 64 * 2;
   static constexpr uint32_t kB = NT * 64 * 2;
   static constexpr uint32_t kStage = kA + kB;
@@ -47,7 +55,7 @@ template <int NT, int EPI, bool A_MN>
 __device__ __forceinline__ void wgemm_body(const CUtensorMap& tmA, const CUtensorMap& tmA2,
                                            const CUtensorMap& tmB, const WgArgs& a, const int mt,
                                            const int nt, const int z, const int ntile) {
-  using C = WgCfg<NT>;
+  using C = WgCfg<NT, EPI>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -326,7 +334,7 @@ __device__ __forceinline__ void wgemm_body(const CUtensorMap& tmA, const CUtenso
 }
 
 template <int NT, int EPI, bool A_MN>
-__global__ void __launch_bounds__(kThreads, WgCfg<NT>::kMinBlocks)
+__global__ void __launch_bounds__(kThreads, (WgCfg<NT, EPI>::kMinBlocks))
 wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
              const __grid_constant__ CUtensorMap tmB, const WgArgs a) {
   wgemm_body<NT, EPI, A_MN>(tmA, tmA2, tmB, a, blockIdx.x, blockIdx.y, blockIdx.z, gridDim.y);
@@ -337,10 +345,10 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 // one waits for nothing of the other.
 template <int NT1, int NT2>
 struct DualCfg {
-  static constexpr int kMinBlocks =
-      WgCfg<NT1>::kMinBlocks < WgCfg<NT2>::kMinBlocks ? WgCfg<NT1>::kMinBlocks : WgCfg<NT2>::kMinBlocks;
-  static constexpr uint32_t kSmem =
-      WgCfg<NT1>::kSmem > WgCfg<NT2>::kSmem ? WgCfg<NT1>::kSmem : WgCfg<NT2>::kSmem;
+  using C1 = WgCfg<NT1, WG_APPEND>;
+  using C2 = WgCfg<NT2, WG_QIMG>;
+  static constexpr int kMinBlocks = C1::kMinBlocks < C2::kMinBlocks ? C1::kMinBlocks : C2::kMinBlocks;
+  static constexpr uint32_t kSmem = C1::kSmem > C2::kSmem ? C1::kSmem : C2::kSmem;
 };
 
 template <int NT1, int NT2>
@@ -398,7 +406,7 @@ cudaError_t launch_dual_nt1(const WgPlan& p1, const WgPlan& p2, cudaStream_t st,
 
 template <int NT, int EPI, bool A_MN>
 cudaError_t launch_nt(const WgPlan& p, cudaStream_t st, bool pdl) {
-  using C = WgCfg<NT>;
+  using C = WgCfg<NT, EPI>;
   auto kern = wgemm_kernel<NT, EPI, A_MN>;
   static std::atomic<uint64_t> attr_done{0};   // per instantiation
   if (const cudaError_t e = smem_attr_once(attr_done, kern, (int)C::kSmem); e != cudaSuccess)
