@@ -242,6 +242,22 @@ def test_two_tokens_equal_two_single_decodes():
     assert _rel(both[0], first[0]) < 1e-13 and _rel(both[1], second[0]) < 1e-13
 
 
+@pytest.mark.parametrize("T", [5, 40])
+def test_chunk_of_tokens_equals_successive_single_decodes(T):
+    """A chunk of T new tokens (prefill) is T single-token decodes, token t
+    seeing the cache up to itself: the causal mask inside the chunk."""
+    dims = SMALL_SHAPES[1]
+    S = 70
+    w, h, q = _rand_case(dims, S, T, seed=7 + T)
+    rows = _rows(dims, w, h)
+    chunk = mla.decode_explicit(dims, rows, q, w, T)["u"]
+    for t in range(T):
+        one = mla.decode_explicit(dims, rows[:S - T + t + 1], q[t:t + 1], w, 1)["u"][0]
+        assert _rel(chunk[t], one) < 1e-12
+    brute_u = brute.decode(dims, h.tolist(), q.tolist(), {k: v.tolist() for k, v in w.items()}, T)
+    assert _rel(chunk, np.array(brute_u)) < 1e-12
+
+
 def test_rope_key_is_shared_and_in_row():
     """k^R occupies columns d_c.. of the row, is the same for every head and
     carries the position (caching only c^KV would lose it)."""
