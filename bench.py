@@ -36,8 +36,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode tokens/s and latent-cache GB/s (% of B300 roofline), 1 GPU"
+METRIC_PREFILL = "MLA prefill tokens/s (a causal chunk of T new tokens per sequence), 1 GPU"
 DEFAULT_STEPS = {"tiny-fp32": 200, "b1-l4096": 1000, "b64-paged": 300, "b4-l128k": 300,
-                 "b128-l16k-t2": 50, "b1-l4096-x60": 30, "b64-paged-x8": 30}
+                 "b128-l16k-t2": 50, "b1-l4096-x60": 30, "b64-paged-x8": 30,
+                 "prefill-b4-t4096": 20, "chunk-b1-l12k-t4096": 20, "prefill-b64-t128": 50}
+PREFILL = ("prefill-b4-t4096", "chunk-b1-l12k-t4096", "prefill-b64-t128")
+FORMS = {"auto": 0, "explicit": 1, "absorbed": 2}
 
 
 # ----------------------------------------------------------------------------- setup
@@ -48,7 +52,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="b128-l16k-t2",
                     choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2",
-                             "b1-l4096-x60", "b64-paged-x8"])
+                             "b1-l4096-x60", "b64-paged-x8"] + list(PREFILL))
+    ap.add_argument("--form", default="auto", choices=list(FORMS),
+                    help="prefill workloads: the attention form mla_prefill uses (auto: the "
+                         "library's choice by FLOPs)")
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--query-path", action="store_true",
                     help="time the step from the hidden states alone (mla_layer_step: the "
@@ -106,8 +113,12 @@ def captured_traffic(config_key: str, kernel: str):
 
 
 # ----------------------------------------------------------------------------- work model
-def work_model(wl, query_path=False):
-    """Algorithmic bytes and FLOPs per launch of each kernel, and per step."""
+def work_model(wl, query_path=False, form="absorbed"):
+    """Algorithmic bytes and FLOPs per launch of each kernel, and per step.
+
+    form="explicit": a prefill chunk in the explicit form (gather the cached
+    rows, up-project K^C and V per head, causal attention over 192 + 128
+    features, W_O); otherwise the absorbed decode kernels."""
     d = wl.dims
     es = 2 if wl.dtype == "bf16" else 4
     M, H, dc, dr, R = wl.B * wl.T, d.n_heads, d.d_latent, d.d_rope, d.row_width
@@ -126,6 +137,21 @@ def work_model(wl, query_path=False):
         "out_proj": (D * H * dv * es + M * H * dv * es + M * D * es, 2.0 * M * D * H * dv),
         "plan": (wl.B * 4, 0.0),
     }
+    if form == "explicit":
+        n = cache_rows
+        k.update({
+            "gather": (2 * n * R * es, 0.0),
+            "key_up": (H * dn * dc * es + n * dc * es + n * H * dn * es, 2.0 * n * H * dn * dc),
+            "value_up": (H * dv * dc * es + n * dc * es + n * H * dv * es,
+                         2.0 * n * H * dv * dc),
+            "rope_q": (2 * M * H * (dn + dr) * es, 0.0),
+            "prefill_attend": (M * H * (dn + dr) * es + n * (H * (dn + dv) + dr) * es
+                               + M * H * dv * es, 2.0 * visible * H * (dn + dr + dv)),
+        })
+        steps = ["compress_append", "gather", "key_up", "value_up", "rope_q", "prefill_attend",
+                 "out_proj"]
+        return (k, sum(k[x][0] for x in steps), sum(k[x][1] for x in steps),
+                cache_rows * R * es)
     # one launch runs the append and the absorbed query together
     k["append_absorb"] = tuple(a + b for a, b in zip(k["compress_append"], k["absorb_q"]))
     tot_bytes = (R * D + H * dn * dc + H * dv * dc + D * H * dv) * es \
@@ -327,6 +353,7 @@ def _cuda():
 
 
 def run_mla(a, wl, rank, local_rank, world):
+    prefill = a.config in PREFILL
     import torch
     import torch.distributed as dist
     import mla_latent_kv_82_b300 as m
@@ -343,6 +370,10 @@ def run_mla(a, wl, rank, local_rank, world):
     else:
         st = DeviceState(wl, device=local_rank, query_path=a.query_path)
         step = st.layer_step if a.query_path else st.step
+        if prefill:
+            form = FORMS[a.form]
+            step = lambda: st.prefill_chunk(form)   # noqa: E731
+            step()   # sizes the prefill workspace outside the captured graph
     torch.cuda.synchronize()
     l2 = getattr(props, "L2_cache_size", 126 << 20) or (126 << 20)
     # L2 flush: write a 2x-L2 buffer, then read another one, so the timed step
@@ -429,7 +460,8 @@ def run_mla(a, wl, rank, local_rank, world):
         m.mla_profile_enable(cx, 0)
 
     # ---- roofline of the dominant kernel and of the whole step
-    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path)
+    resolved = "explicit" if "prefill_attend" in kt else "absorbed"
+    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path, resolved)
     avg = {k: sum(v) / len(v) for k, v in kt.items() if v}
     share = {k: sum(v) for k, v in kt.items()}
     dom = max(share, key=share.get)
@@ -500,8 +532,22 @@ def run_mla(a, wl, rank, local_rank, world):
 
     if rank != 0:
         return None
+    if prefill:
+        graph = (f"each step is one CUDA-graph replay of mla_prefill (form {a.form}: "
+                 f"{resolved} ran): append the chunk's rows, then causal attention and W_O")
+    elif wl.layers > 1:
+        graph = ("each step is one CUDA-graph replay of mla_multi_layer_step "
+                 f"through {wl.layers} layers (each: queries from its input, "
+                 "append, decode, residual)")
+    elif a.query_path:
+        graph = ("each step is one CUDA-graph replay of mla_layer_step (queries "
+                 "from the new hidden states, append, decode)")
+    else:
+        graph = ("each step is one CUDA-graph replay of mla_append_decode "
+                 "(append the new rows, then decode them)")
     return {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC_PREFILL if prefill else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
@@ -509,16 +555,11 @@ def run_mla(a, wl, rank, local_rank, world):
         "config": {"workload": wl.name + ("+query-path" if a.query_path and wl.layers == 1
                                           else ""),
                    "batch": wl.B, "T": wl.T, "layers": wl.layers,
+                   **({"form": a.form, "form_ran": resolved} if prefill else {}),
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
                    f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
                    "step's event bracket)",
-                   "graph": ("each step is one CUDA-graph replay of mla_multi_layer_step "
-                             f"through {wl.layers} layers (each: queries from its input, "
-                             "append, decode, residual)") if wl.layers > 1 else
-                            ("each step is one CUDA-graph replay of mla_layer_step (queries "
-                             "from the new hidden states, append, decode)") if a.query_path else
-                            ("each step is one CUDA-graph replay of mla_append_decode "
-                             "(append the new rows, then decode them)"),
+                   "graph": graph,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "cache_gbs": cache_bytes / t_step / 1e9,
                    "step_algorithmic_gb": tot_bytes / 1e9,

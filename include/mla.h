@@ -189,6 +189,46 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
                           int T, void* out, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* Prefill: the new tokens come in chunks of T per sequence (T up to 4096),
+ * appended and attended to with the causal mask inside the chunk: the
+ * results are those of mla_append_decode of the same T tokens.  The pages
+ * warn that the absorbed form is not always the fastest
+ * (www.pptc.cn/news/140720 §6 问题三): recovering K and V pays off when many
+ * queries share them.  `form` chooses how the attention is computed:
+ *   MLA_FORM_ABSORBED  the decode path (W^UK folded into the queries, every
+ *                      query scoring the 576-wide rows directly);
+ *   MLA_FORM_EXPLICIT  K^C_i = W^UK_i c and V_i = W^UV_i c for every cached
+ *                      row, then per-head causal attention over
+ *                      [K^C_i ; k^R] (192 features) and V_i (bf16 only);
+ *   MLA_FORM_AUTO      the form with fewer FLOPs for this shape: explicit
+ *                      when 2·2·512·(n_h·d_h) per key (the up-projections)
+ *                      plus 2·n_h·(192+128) per (query, key) is below
+ *                      2·n_h·(576+512) per (query, key), i.e. for chunks of
+ *                      about 170 tokens and more (S taken as
+ *                      max_pages·page_size); fp32 contexts, and calls whose
+ *                      batch·max_pages·page_size exceeds 2^18 rows, use the
+ *                      absorbed form.
+ * Arguments as for mla_append_decode (q: [batch, T, n_heads, 192]) with
+ * T <= 4096 and batch·T <= 32768; the workspace must hold
+ * mla_prefill_workspace_size bytes (MLA_ERR_WORKSPACE otherwise).  The
+ * explicit form's buffers: the gathered rows, K^C and V of every row of
+ * the batch (batch·max_pages·page_size rows of 1152 + 2·32768 bytes), the
+ * rotated queries and the per-head outputs.  MLA_ERR_UNSUPPORTED for
+ * MLA_FORM_EXPLICIT on an fp32 context, MLA_ERR_INVALID_ARG for it past
+ * the row bound.  Device-side index errors are reported as for
+ * mla_append_decode. */
+enum { MLA_FORM_AUTO = 0, MLA_FORM_EXPLICIT = 1, MLA_FORM_ABSORBED = 2 };
+
+size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T,
+                                  int max_pages);
+
+mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions,
+                       const void* q, void* cache, int num_pages,
+                       const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens, int batch, int T, int form,
+                       void* out, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
 /* One decode step through a stack of n_layers attention layers, each with
  * its own context (weights, d_cq > 0) and its own cache pool; the pools
  * share one page layout (block_table, num_pages).  The pages count the cache

@@ -24,13 +24,16 @@ MLA_ERR_TIMEOUT = 5
 MLA_ERR_DEVICE_INDEX = 6
 MLA_BF16 = 0
 MLA_FP32 = 1
+MLA_FORM_AUTO = 0
+MLA_FORM_EXPLICIT = 1
+MLA_FORM_ABSORBED = 2
 
 EXPORTED = (
     "mla_create", "mla_destroy", "mla_compress_append", "mla_decode_workspace_size",
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
     "mla_decode_static_workspace", "mla_append_decode", "mla_layer_step",
-    "mla_multi_layer_step",
+    "mla_multi_layer_step", "mla_prefill_workspace_size", "mla_prefill",
 )
 
 
@@ -80,6 +83,8 @@ def _load() -> ctypes.CDLL:
         "mla_decode_static_workspace": ([vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp], i32),
         "mla_append_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp],
                               i32),
+        "mla_prefill_workspace_size": ([vp, i32, i32, i32], sz),
+        "mla_prefill": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, vp, vp, sz, vp], i32),
         "mla_layer_step": ([vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp], i32),
         "mla_multi_layer_step": ([ctypes.POINTER(vp), i32, vp, vp, ctypes.POINTER(vp), i32, vp,
                                   i32, vp, i32, i32, vp, vp, sz, vp], i32),
@@ -139,6 +144,16 @@ def mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_p
                       batch, T, out, workspace, workspace_bytes, stream) -> int:
     return _lib.mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_pages,
                                   seq_lens, batch, T, out, workspace, workspace_bytes, stream)
+
+
+def mla_prefill_workspace_size(ctx, batch, T, max_pages) -> int:
+    return _lib.mla_prefill_workspace_size(ctx, batch, T, max_pages)
+
+
+def mla_prefill(ctx, h, positions, q, cache, num_pages, block_table, max_pages, seq_lens, batch,
+                T, form, out, workspace, workspace_bytes, stream) -> int:
+    return _lib.mla_prefill(ctx, h, positions, q, cache, num_pages, block_table, max_pages,
+                            seq_lens, batch, T, form, out, workspace, workspace_bytes, stream)
 
 
 def mla_layer_step(ctx, h, positions, cache, num_pages, block_table, max_pages, seq_lens, batch,
@@ -261,6 +276,20 @@ class MLA:
                                self._stream(stream))
         if st != MLA_OK:
             raise MLAError(st, "mla_append_decode")
+
+    def prefill_workspace_size(self, batch: int, T: int, max_pages: int) -> int:
+        return mla_prefill_workspace_size(self.ctx, batch, T, max_pages)
+
+    def prefill(self, h, positions, q, cache, block_table, seq_lens, out, workspace,
+                form=MLA_FORM_AUTO, stream=None):
+        batch, T = q.shape[0], q.shape[1]
+        st = mla_prefill(self.ctx, h.data_ptr(), positions.data_ptr(), q.data_ptr(),
+                         cache.data_ptr(), cache.shape[0] // self.dims.page_size,
+                         block_table.data_ptr(), block_table.shape[-1], seq_lens.data_ptr(),
+                         batch, T, form, out.data_ptr(), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), self._stream(stream))
+        if st != MLA_OK:
+            raise MLAError(st, "mla_prefill")
 
     def layer_step(self, h, positions, cache, block_table, seq_lens, out, workspace,
                    stream=None):

@@ -1,4 +1,5 @@
 // C ABI: argument validation, context, RoPE table and dispatch.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -323,6 +324,94 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
     mla::f32_decode(ctx, reinterpret_cast<const float*>(ws + L.q_in),
                     static_cast<const float*>(cache), num_pages, block_table, max_pages, batch, T,
                     static_cast<float*>(out), ws, L, st);
+  }
+  mla::prof_mark(ctx, st, nullptr);
+  if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  return launch_status();
+}
+
+// The explicit form holds the up-projected keys and values of every cached
+// row (32 KB per row): at most this many rows per call.
+constexpr long long kExplicitRows = 1LL << 18;
+
+static bool explicit_fits(const mla_ctx* ctx, int batch, int max_pages) {
+  return ctx->cfg.dtype == MLA_BF16 &&
+         (long long)batch * max_pages * ctx->cfg.page_size <= kExplicitRows;
+}
+
+size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T, int max_pages) {
+  if (!ctx || batch < 1 || T < 1 || max_pages < 1) return 0;
+  size_t n = mla::workspace_layout(ctx, batch, T, max_pages).total;
+  if (explicit_fits(ctx, batch, max_pages))
+    n = std::max(n, mla::prefill_layout(ctx, batch, T, max_pages).total);
+  return n;
+}
+
+// FLOPs of the two forms for T queries per sequence against up to S keys.
+static bool explicit_is_cheaper(const mla_config& c, int T, long long S) {
+  const double H = c.n_heads;
+  const double up = 2.0 * 2.0 * c.d_latent * H * c.d_nope * (double)S;
+  const double expl = up + 2.0 * H * (c.d_nope + c.d_rope + c.d_v) * (double)T * (double)S;
+  const double absd = 2.0 * H * (c.d_latent + c.d_rope + c.d_latent) * (double)T * (double)S;
+  return expl < absd;
+}
+
+mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions, const void* q,
+                       void* cache, int num_pages, const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens, int batch, int T, int form, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ctx || !h || !positions || !q || !cache || !block_table || !seq_lens || !out ||
+      !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (batch < 1 || T < 1 || T > 4096 || max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if ((long long)batch * max_pages > (1LL << 30) || (long long)batch * T > 32768)
+    return MLA_ERR_INVALID_ARG;
+  if (form < MLA_FORM_AUTO || form > MLA_FORM_ABSORBED) return MLA_ERR_INVALID_ARG;
+  const bool bf = ctx->cfg.dtype == MLA_BF16;
+  if (!bf && form == MLA_FORM_EXPLICIT) return MLA_ERR_UNSUPPORTED;
+  if (form == MLA_FORM_EXPLICIT && !explicit_fits(ctx, batch, max_pages))
+    return MLA_ERR_INVALID_ARG;
+  const size_t a = bf ? 16 : 4;
+  if (!aligned(h, a) || !aligned(q, a) || !aligned(cache, a) || !aligned(out, a) ||
+      !aligned(workspace, 256) || !aligned(positions, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < mla_prefill_workspace_size(ctx, batch, T, max_pages))
+    return MLA_ERR_WORKSPACE;
+  const bool expl = form == MLA_FORM_EXPLICIT ||
+                    (form == MLA_FORM_AUTO && explicit_fits(ctx, batch, max_pages) &&
+                     explicit_is_cheaper(ctx->cfg, T, (long long)max_pages * ctx->cfg.page_size));
+  DeviceGuard g(ctx->device);
+  if (!g.ok) return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  bool launched = true;
+  if (expl) {
+    const mla::PrefillLayout L = mla::prefill_layout(ctx, batch, T, max_pages);
+    launched = mla::bf16_compress_append(ctx, static_cast<const __nv_bfloat16*>(h), batch, T,
+                                         positions, block_table, max_pages,
+                                         static_cast<__nv_bfloat16*>(cache), num_pages, st) &&
+               mla::bf16_prefill_explicit(ctx, static_cast<const __nv_bfloat16*>(q),
+                                          static_cast<const __nv_bfloat16*>(cache), num_pages,
+                                          block_table, max_pages, seq_lens, batch, T,
+                                          static_cast<__nv_bfloat16*>(out), ws, L, st);
+  } else {
+    const mla::WsLayout L = mla::workspace_layout(ctx, batch, T, max_pages);
+    if (bf) {
+      launched = mla::bf16_append_decode(
+          ctx, static_cast<const __nv_bfloat16*>(h), positions,
+          static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(cache), num_pages,
+          block_table, max_pages, seq_lens, batch, T, static_cast<__nv_bfloat16*>(out), ws, L, st);
+    } else {
+      mla::f32_compress_append(ctx, static_cast<const float*>(h), batch, T, positions, block_table,
+                               max_pages, static_cast<float*>(cache), num_pages, st);
+      mla::prof_mark(ctx, st, "plan");
+      mla::launch_plan(ctx, L, ws, seq_lens, batch, T, max_pages, st);
+      ctx->launches += 1;
+      mla::f32_decode(ctx, static_cast<const float*>(q), static_cast<const float*>(cache),
+                      num_pages, block_table, max_pages, batch, T, static_cast<float*>(out), ws,
+                      L, st);
+    }
   }
   mla::prof_mark(ctx, st, nullptr);
   if (!launched) { cudaGetLastError(); return MLA_ERR_CUDA; }

@@ -1,5 +1,5 @@
-// Pieces shared by the split-KV attention kernels (attend_tc.cu, one CTA
-// per query token, and attend_pair.cu, two query tokens per CTA pair):
+// Pieces shared by the attention kernels (attend_sv.cu, the split-KV
+// latent attention, and prefill.cu, the per-head causal attention):
 // segment iteration over a split's pages, pool-row lookup, stale-row
 // zeroing, the softmax arithmetic on a 128-token score row, warp-uniform
 // bounded waits and ring positions.

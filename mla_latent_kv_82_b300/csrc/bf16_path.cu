@@ -243,6 +243,7 @@ bool bf16_setup(mla_ctx* ctx) {
   bool ok = make_tmap_bf16_2d(&ctx->tm_wdkv, w.w_dkv, kLat, D, D, 64, 128, true) &&
             make_tmap_bf16_2d(&ctx->tm_wkr, w.w_kr, kRope, D, D, 64, 128, true) &&
             make_tmap_bf16_2d(&ctx->tm_wuk, w.w_uk, kHeads * kNope, kLat, kLat, 64, 64, true) &&
+            make_tmap_bf16_2d(&ctx->tm_wuk_rows, w.w_uk, kHeads * kNope, kLat, kLat, 64, 128, true) &&
             make_tmap_bf16_2d(&ctx->tm_wuv, w.w_uv, kHeads * kDv, kLat, kLat, 64, 128, true) &&
             make_tmap_bf16_2d(&ctx->tm_wo, w.w_o, D, kHeads * kDv, kHeads * kDv, 64, 128, true);
   if (ok && ctx->cfg.d_cq > 0) {
@@ -519,6 +520,47 @@ bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsL
   // q^C -> q[:, head, 0..127]
   return rowmajor(bp.uq, kHeads, ctx->tm_wuq, cq, dcq, dcq / 64, 1, kNope, q, kQRow,
                   kNope + kRope, 0, "query_up");
+}
+
+// out[t, f] = sum_k W[f, k] x[t, k] for the m_tiles * 128 rows of the weight
+// map and k_chunks * 64 columns of x ([M, x_cols] row-major), out row-major
+// with leading dimension ld_out.
+bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int k_chunks,
+                        const __nv_bfloat16* x, int M, int x_cols, __nv_bfloat16* out,
+                        int ld_out, float* part, cudaStream_t st, const char* name) {
+  const GemmShape g = gemm_shape(ctx, M, m_tiles, k_chunks, 4, kSplitCap);
+  if (g.n_tiles > 65535 || (g.splits > 1 && (long long)m_tiles * g.n_tiles > kCounters))
+    return false;
+  WgPlan p{};
+  p.nt = g.nt;
+  p.n_tiles = g.n_tiles;
+  p.m_tiles = m_tiles;
+  p.tmA = wmap;
+  p.tmA2 = wmap;
+  if (!make_tmap_bf16_2d(&p.tmB, x, M, x_cols, x_cols, 64, p.nt, false)) {
+    cudaGetLastError();
+    return false;
+  }
+  WgArgs& a = p.args;
+  a = base_args(ctx);
+  a.n_tokens = M;
+  a.k_chunks = k_chunks;
+  a.splits = g.splits;
+  a.tiles_per_head = m_tiles;
+  a.out = out;
+  a.ld_out = ld_out;
+  a.out_head_cols = 0;
+  a.partials = part;
+  prof_mark(ctx, st, name);
+  ctx->launches += 1;
+  return check(wgemm_launch(p, WG_ROWMAJOR, false, st, true));
+}
+
+size_t prefill_partial_bytes(const mla_ctx* ctx, int R, int M) {
+  const int D = ctx->cfg.d_model;
+  const GemmShape kv = gemm_shape(ctx, R, kHeads, kLat / 64, 4, kSplitCap);
+  const GemmShape o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap);
+  return std::max(partial_bytes(kv, kHeads), partial_bytes(o, D / 128));
 }
 
 bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos,

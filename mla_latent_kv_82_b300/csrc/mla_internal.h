@@ -22,6 +22,7 @@ struct mla_ctx {
   int64_t launches;
   // bf16 path: TMA maps of the weights, split-K scratch of the append
   CUtensorMap tm_wdkv, tm_wkr, tm_wuk, tm_wuv, tm_wo;
+  CUtensorMap tm_wuk_rows;              // W^UK with 128-row boxes (K^C = W^UK c)
   CUtensorMap tm_wdq, tm_wuq, tm_wqr;   // query path (d_cq > 0)
   float* append_partials = nullptr;   // kAppendPartialBytes
   int* counters = nullptr;            // kCounters, zero between launches
@@ -92,7 +93,28 @@ bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos
                         const int32_t* bt, int max_pages, const int32_t* seq_lens, int B, int T,
                         __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st);
 
-// Query path of mla_layer_step: q = [W^UQ W^DQ h ; W^QR h] per head into
+// Prefill in the explicit form (prefill.cu): byte layout of its workspace.
+struct PrefillLayout {
+  int Smax;        // rows per sequence in the gathered buffers (max_pages * page)
+  size_t rows;     // bf16 [B*Smax, 576] the cached rows of every sequence, zero padded
+  size_t k;        // bf16 [B*Smax, n_heads*d_nope] K^C = W^UK c
+  size_t v;        // bf16 [B*Smax, n_heads*d_v] V = W^UV c
+  size_t q_rot;    // bf16 [B*T, n_heads, d_nope + d_rope] queries with q^R rotated
+  size_t o;        // bf16 [B*T, n_heads*d_v]
+  size_t wg_part;  // fp32 split-K partials
+  size_t total;
+};
+PrefillLayout prefill_layout(const mla_ctx* ctx, int B, int T, int max_pages);
+size_t prefill_partial_bytes(const mla_ctx* ctx, int R, int M);
+bool bf16_prefill_explicit(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+                           int num_pages, const int32_t* bt, int max_pages,
+                           const int32_t* seq_lens, int B, int T, __nv_bfloat16* out, char* ws,
+                           const PrefillLayout& L, cudaStream_t st);
+bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int k_chunks,
+                        const __nv_bfloat16* x, int M, int x_cols, __nv_bfloat16* out,
+                        int ld_out, float* part, cudaStream_t st, const char* name);
+
+// Query path of mla_layer_step:// Query path of mla_layer_step: q = [W^UQ W^DQ h ; W^QR h] per head into
 // the workspace's q_in (layout of mla_decode's q).
 bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsLayout& L,
                 cudaStream_t st);

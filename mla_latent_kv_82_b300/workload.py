@@ -99,6 +99,17 @@ class DeviceState:
         self.mla.layer_step(self.h_new, self.pos_new, self.cache, self.bt, self.seq_lens,
                             self.out, self.ws, stream=stream)
 
+    def prefill_chunk(self, form: int = 0, stream=None):
+        """The T new tokens of every sequence as one prefill chunk
+        (mla_prefill): appended, then attended to with the causal mask, in
+        `form` (MLA_FORM_AUTO, _EXPLICIT or _ABSORBED)."""
+        need = self.mla.prefill_workspace_size(self.wl.B, self.wl.T, self.bt.shape[1])
+        if need > self.ws_bytes:
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.dev)
+            self.ws_bytes = need
+        self.mla.prefill(self.h_new, self.pos_new, self.q, self.cache, self.bt, self.seq_lens,
+                         self.out, self.ws, form=form, stream=stream)
+
     def step_separate(self, stream=None):
         """The same step as two calls: mla_compress_append, then mla_decode."""
         self.append_new(stream)

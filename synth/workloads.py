@@ -173,8 +173,15 @@ def config(name: str) -> Workload:
     if name == "b64-paged-x8":   # the batch-64 paged step through 8 layers
         return Workload("v2-b64-paged-Lrand-x8layers", V2, "bf16", paged_lens(), 1, True,
                         layers=8)
+    if name == "prefill-b4-t4096":   # four 4096-token prompts, one chunk each
+        return Workload("v2-prefill-b4-T4096", V2, "bf16", [0] * 4, 4096, False)
+    if name == "chunk-b1-l12k-t4096":   # the last 4096-token chunk of a 16K prompt
+        return Workload("v2-chunk-b1-L12288-T4096", V2, "bf16", [12288], 4096, False)
+    if name == "prefill-b64-t128":   # 64 short prompts of 128 tokens, shuffled pages
+        return Workload("v2-prefill-b64-T128", V2, "bf16", [0] * 64, 128, True)
     raise KeyError(name)
 
 
 CONFIG_NAMES = ("tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2",
                 "b1-l4096-x60", "b64-paged-x8")
+PREFILL_NAMES = ("prefill-b4-t4096", "chunk-b1-l12k-t4096", "prefill-b64-t128")

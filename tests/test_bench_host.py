@@ -138,3 +138,24 @@ def test_work_model_layer_stack():
     assert b60 == 60 * (b1 + 3 * 5120 * 2)
     assert f60 == 60 * (f1 + 5120)
     assert c60 == 60 * c1 == 60 * 4096 * 576 * 2
+
+
+def test_work_model_prefill_explicit():
+    """The explicit prefill form: K^C and V of every cached row up-projected
+    once (2 * 512 * 16384 FLOP each), 2 * (192 + 128) FLOP per head and
+    visible (query, key) pair, and the causal count T (T + 1) / 2 for a chunk
+    with an empty prefix."""
+    from synth import workloads as W
+    wl = W.config("prefill-b4-t4096")
+    k, b, f, c = bench.work_model(wl, form="explicit")
+    n = 4 * 4096
+    assert k["key_up"][1] == k["value_up"][1] == 2 * n * 16384 * 512
+    assert k["prefill_attend"][1] == 2 * (4 * 4096 * 4097 // 2) * 128 * (192 + 128)
+    assert k["gather"][0] == 2 * n * 576 * 2
+    assert f == sum(k[x][1] for x in ("compress_append", "key_up", "value_up", "prefill_attend",
+                                      "out_proj"))
+    assert c == n * 576 * 2
+    # the same chunk in the absorbed form: 2 * (576 + 512) FLOP per pair
+    ka, _, fa, _ = bench.work_model(wl)
+    assert ka["attend"][1] == 2 * (4 * 4096 * 4097 // 2) * 128 * (576 + 512)
+    assert fa > f
