@@ -200,14 +200,7 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
  *   MLA_FORM_EXPLICIT  K^C_i = W^UK_i c and V_i = W^UV_i c for every cached
  *                      row, then per-head causal attention over
  *                      [K^C_i ; k^R] (192 features) and V_i (bf16 only);
- *   MLA_FORM_AUTO      the form with fewer FLOPs for this shape: explicit
- *                      when 2·2·512·(n_h·d_h) per key (the up-projections)
- *                      plus 2·n_h·(192+128) per (query, key) is below
- *                      2·n_h·(576+512) per (query, key), i.e. for chunks of
- *                      about 170 tokens and more (S taken as
- *                      max_pages·page_size); fp32 contexts, and calls whose
- *                      batch·max_pages·page_size exceeds 2^18 rows, use the
- *                      absorbed form.
+ *   MLA_FORM_AUTO      the form mla_prefill_form names for this shape.
  * Arguments as for mla_append_decode (q: [batch, T, n_heads, 192]) with
  * T <= 4096 and batch·T <= 32768; the workspace must hold
  * mla_prefill_workspace_size bytes (MLA_ERR_WORKSPACE otherwise).  The
@@ -221,6 +214,19 @@ enum { MLA_FORM_AUTO = 0, MLA_FORM_EXPLICIT = 1, MLA_FORM_ABSORBED = 2 };
 
 size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T,
                                   int max_pages);
+
+/* The form MLA_FORM_AUTO takes for this shape (MLA_FORM_EXPLICIT or
+ * MLA_FORM_ABSORBED; -1 for invalid arguments): the one with the smaller
+ * estimated time, from per-unit costs of the two forms' kernels measured on
+ * B300 at DeepSeek-V2 widths.  The explicit form pays per cached key (the
+ * K^C and V up-projections, 2·2·512·16384 FLOP) and less per (query, key)
+ * pair (2·n_h·320 FLOP against 2·n_h·1088); the absorbed form pays per query
+ * token (absorbed query, combine, W^UV).  With S = max_pages·page_size keys
+ * per sequence: the explicit form for prompts on an empty cache from a few
+ * dozen tokens up, the absorbed form for decode and for short chunks after
+ * a long prefix (below about 460 tokens after 12288).  fp32 contexts, and calls whose batch·max_pages·page_size exceeds
+ * 2^18 rows, always get MLA_FORM_ABSORBED. */
+int mla_prefill_form(const mla_ctx* ctx, int batch, int T, int max_pages);
 
 mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions,
                        const void* q, void* cache, int num_pages,

@@ -33,7 +33,7 @@ EXPORTED = (
     "mla_decode", "mla_decode_workspace_offsets", "mla_check_status", "mla_launch_count",
     "mla_selftest_bounded_wait", "mla_status_string", "mla_profile_enable", "mla_profile_read",
     "mla_decode_static_workspace", "mla_append_decode", "mla_layer_step",
-    "mla_multi_layer_step", "mla_prefill_workspace_size", "mla_prefill",
+    "mla_multi_layer_step", "mla_prefill_workspace_size", "mla_prefill", "mla_prefill_form",
 )
 
 
@@ -84,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "mla_append_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp],
                               i32),
         "mla_prefill_workspace_size": ([vp, i32, i32, i32], sz),
+        "mla_prefill_form": ([vp, i32, i32, i32], i32),
         "mla_prefill": ([vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, vp, vp, sz, vp], i32),
         "mla_layer_step": ([vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, vp, vp, sz, vp], i32),
         "mla_multi_layer_step": ([ctypes.POINTER(vp), i32, vp, vp, ctypes.POINTER(vp), i32, vp,
@@ -148,6 +149,10 @@ def mla_append_decode(ctx, h, positions, q, cache, num_pages, block_table, max_p
 
 def mla_prefill_workspace_size(ctx, batch, T, max_pages) -> int:
     return _lib.mla_prefill_workspace_size(ctx, batch, T, max_pages)
+
+
+def mla_prefill_form(ctx, batch, T, max_pages) -> int:
+    return _lib.mla_prefill_form(ctx, batch, T, max_pages)
 
 
 def mla_prefill(ctx, h, positions, q, cache, num_pages, block_table, max_pages, seq_lens, batch,
@@ -279,6 +284,9 @@ class MLA:
 
     def prefill_workspace_size(self, batch: int, T: int, max_pages: int) -> int:
         return mla_prefill_workspace_size(self.ctx, batch, T, max_pages)
+
+    def prefill_form(self, batch: int, T: int, max_pages: int) -> int:
+        return mla_prefill_form(self.ctx, batch, T, max_pages)
 
     def prefill(self, h, positions, q, cache, block_table, seq_lens, out, workspace,
                 form=MLA_FORM_AUTO, stream=None):

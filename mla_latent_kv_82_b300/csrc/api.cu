@@ -347,13 +347,31 @@ size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T, int max_
   return n;
 }
 
-// FLOPs of the two forms for T queries per sequence against up to S keys.
-static bool explicit_is_cheaper(const mla_config& c, int T, long long S) {
-  const double H = c.n_heads;
-  const double up = 2.0 * 2.0 * c.d_latent * H * c.d_nope * (double)S;
-  const double expl = up + 2.0 * H * (c.d_nope + c.d_rope + c.d_v) * (double)T * (double)S;
-  const double absd = 2.0 * H * (c.d_latent + c.d_rope + c.d_latent) * (double)T * (double)S;
+// Estimated time of the two forms for `batch` sequences of T new tokens
+// each against up to S keys, from per-unit costs of this library's kernels
+// measured on B300 at DeepSeek-V2 widths (ns).  Explicit: 65 per cached key
+// (gather, K^C and V up-projections), 16 per query token (rotated queries),
+// 0.11 per visible (query, key) pair (2·128·320 FLOP).  Absorbed: 190 per
+// query token (absorbed query, combine, W^UV) and 0.24 per pair
+// (2·128·1088 FLOP).  The append and W_O are common to both.
+static bool explicit_is_cheaper(int batch, int T, long long S) {
+  const double B = batch, t = T, s = (double)S;
+  const double pairs = B * t * (s - 0.5 * (t - 1.0));
+  const double expl = 65.0 * B * s + 16.0 * B * t + 0.11 * pairs;
+  const double absd = 190.0 * B * t + 0.24 * pairs;
   return expl < absd;
+}
+
+static int prefill_form(const mla_ctx* ctx, int batch, int T, int max_pages) {
+  return explicit_fits(ctx, batch, max_pages) &&
+                 explicit_is_cheaper(batch, T, (long long)max_pages * ctx->cfg.page_size)
+             ? MLA_FORM_EXPLICIT
+             : MLA_FORM_ABSORBED;
+}
+
+int mla_prefill_form(const mla_ctx* ctx, int batch, int T, int max_pages) {
+  if (!ctx || batch < 1 || T < 1 || max_pages < 1) return -1;
+  return prefill_form(ctx, batch, T, max_pages);
 }
 
 mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions, const void* q,
@@ -379,8 +397,8 @@ mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions, co
   if (workspace_bytes < mla_prefill_workspace_size(ctx, batch, T, max_pages))
     return MLA_ERR_WORKSPACE;
   const bool expl = form == MLA_FORM_EXPLICIT ||
-                    (form == MLA_FORM_AUTO && explicit_fits(ctx, batch, max_pages) &&
-                     explicit_is_cheaper(ctx->cfg, T, (long long)max_pages * ctx->cfg.page_size));
+                    (form == MLA_FORM_AUTO &&
+                     prefill_form(ctx, batch, T, max_pages) == MLA_FORM_EXPLICIT);
   DeviceGuard g(ctx->device);
   if (!g.ok) return MLA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

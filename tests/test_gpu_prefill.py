@@ -133,3 +133,33 @@ def test_v2_widths_forms_agree():
         torch.cuda.empty_cache()
     s = omla.error_stats(outs["explicit"], outs["absorbed"])
     assert s["max_rel"] <= 2e-2 and s["mean_rel"] <= 5e-3, s
+
+
+def test_automatic_form_choice():
+    """mla_prefill_form names the form MLA_FORM_AUTO runs: the explicit form
+    for prompts on an empty cache, the absorbed form for decode-sized chunks
+    and for short chunks after a long prefix; an automatic call launches the
+    kernels of the form it names."""
+    import mla_latent_kv_82_b300 as m
+    from mla_latent_kv_82_b300.workload import DeviceState
+    E, A = m.MLA_FORM_EXPLICIT, m.MLA_FORM_ABSORBED
+    st = DeviceState(small_bf16([0], 128))
+    f = st.mla.prefill_form
+    assert f(1, 128, 2) == E          # a 128-token prompt
+    assert f(4, 4096, 64) == E        # four 4096-token prompts
+    assert f(1, 1, 64) == A           # one token
+    assert f(128, 2, 257) == A        # batched decode on 16K caches
+    assert f(1, 256, 200) == A        # 256 tokens after a 12544-token prefix
+    assert f(1, 1024, 208) == E       # 1024 tokens after 12288
+    assert f(64, 128, 8192) == A      # past the explicit form's row bound
+    assert f(1, 0, 2) == -1
+    counts = {}
+    for form in (m.MLA_FORM_AUTO, E, A):
+        n0 = st.mla.launch_count()
+        st.prefill_chunk(form)
+        counts[form] = st.mla.launch_count() - n0
+    torch.cuda.synchronize()
+    assert st.mla.check_status() == 0
+    assert counts[m.MLA_FORM_AUTO] == counts[E] != counts[A]
+    f32 = DeviceState(tiny_f32([0], 40))
+    assert f32.mla.prefill_form(1, 40, 1) == A
