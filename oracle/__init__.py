@@ -7,11 +7,14 @@ and reference legs import this package.  The CUDA library
 * ``oracle.mla``   -- vectorised float64 explicit and absorbed decode,
                       paged addressing, cache-size closed forms;
 * ``oracle.brute`` -- pure-Python scalar decode for tiny inputs;
+* ``oracle.fp8``   -- the E4M3 codec and the row quantiser of the FP8
+                      cache (the decode over its dequantised rows is
+                      ``oracle.mla`` unchanged);
 * ``oracle.case``  -- assembles a workload's inputs (from ``synth``) and
                       runs the oracle on whole sequences or samples.
 
-Parity pins live in ``tests/test_oracle.py``.  Nothing here is "parity
+Parity pins live in ``tests/test_oracle.py`` and ``tests/test_oracle_fp8.py``.  Nothing here is "parity
 unpinned": every function above is checked there against closed forms,
 brute force, special cases or invariants.
 """
-from . import mla, brute  # noqa: F401
+from . import mla, brute, fp8  # noqa: F401
