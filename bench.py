@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--config", default="b128-l16k-t2",
                     choices=["tiny-fp32", "b1-l4096", "b64-paged", "b4-l128k", "b128-l16k-t2",
                              "b1-l4096-x60", "b64-paged-x8"] + list(PREFILL))
+    ap.add_argument("--kv", default="native", choices=["native", "fp8"],
+                    help="latent-cache storage: the context dtype, or E4M3 rows of 656 bytes "
+                         "(bf16 workloads)")
     ap.add_argument("--form", default="auto", choices=list(FORMS),
                     help="prefill workloads: the attention form mla_prefill uses (auto: the "
                          "library's choice by FLOPs)")
@@ -113,7 +116,7 @@ def captured_traffic(config_key: str, kernel: str):
 
 
 # ----------------------------------------------------------------------------- work model
-def work_model(wl, query_path=False, form="absorbed"):
+def work_model(wl, query_path=False, form="absorbed", kv="native"):
     """Algorithmic bytes and FLOPs per launch of each kernel, and per step.
 
     form="explicit": a prefill chunk in the explicit form (gather the cached
@@ -165,6 +168,14 @@ def work_model(wl, query_path=False, form="absorbed"):
         # the queries are no longer an input: their weights are read instead
         tot_bytes += (cq * D + H * dn * cq + H * dr * D) * es - M * H * (dn + dr) * es
         steps += ["query_down", "query_rope", "query_up"]
+    if kv == "fp8":
+        # E4M3 rows of 656 bytes in place of 576 bf16 values; the append
+        # stages bf16 rows that f8_prepare quantises, with the query images
+        R8, Q8 = 656, 82432
+        k["f8_prepare"] = (M * R * es + M * R8 + M * H * R * es + M * Q8, 0.0)
+        k["attend"] = (cache_rows * R8 + M * Q8, 2.0 * visible * H * (R + dc))
+        tot_bytes += cache_rows * (R8 - R * es) + k["f8_prepare"][0]
+        steps.append("f8_prepare")
     tot_flops = sum(k[n][1] for n in steps)
     if wl.layers > 1:
         # every layer reads its own weights and cache; the residual reads h and
@@ -172,8 +183,8 @@ def work_model(wl, query_path=False, form="absorbed"):
         k["residual"] = (3 * M * D * es, 1.0 * M * D)
         tot_bytes = (tot_bytes + k["residual"][0]) * wl.layers
         tot_flops = (tot_flops + k["residual"][1]) * wl.layers
-        return k, tot_bytes, tot_flops, cache_rows * R * es * wl.layers
-    return k, tot_bytes, tot_flops, cache_rows * R * es
+        return k, tot_bytes, tot_flops, cache_rows * (656 if kv == "fp8" else R * es) * wl.layers
+    return k, tot_bytes, tot_flops, cache_rows * (656 if kv == "fp8" else R * es)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -368,7 +379,7 @@ def run_mla(a, wl, rank, local_rank, world):
         st = StackState(wl, device=local_rank)
         step = st.step
     else:
-        st = DeviceState(wl, device=local_rank, query_path=a.query_path)
+        st = DeviceState(wl, device=local_rank, query_path=a.query_path, kv=a.kv)
         step = st.layer_step if a.query_path else st.step
         if prefill:
             form = FORMS[a.form]
@@ -461,7 +472,7 @@ def run_mla(a, wl, rank, local_rank, world):
 
     # ---- roofline of the dominant kernel and of the whole step
     resolved = "explicit" if "prefill_attend" in kt else "absorbed"
-    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path, resolved)
+    kmodel, tot_bytes, tot_flops, cache_bytes = work_model(wl, a.query_path, resolved, a.kv)
     avg = {k: sum(v) / len(v) for k, v in kt.items() if v}
     share = {k: sum(v) for k, v in kt.items()}
     dom = max(share, key=share.get)
@@ -556,6 +567,8 @@ def run_mla(a, wl, rank, local_rank, world):
                                           else ""),
                    "batch": wl.B, "T": wl.T, "layers": wl.layers,
                    **({"form": a.form, "form_ran": resolved} if prefill else {}),
+                   "kv": "E4M3 rows of 656 bytes (per-row scale)" if a.kv == "fp8"
+                         else "rows in the context dtype",
                    "cache_tokens": sum(wl.seq_lens), "l2": "flushed before every timed step "
                    f"(write {2 * l2 >> 20} MiB, then read {2 * l2 >> 20} MiB; outside the "
                    "step's event bracket)",

@@ -84,7 +84,26 @@ typedef struct {
    * bf16 contexts need a multiple of 128 (<= 16384); fp32 any width
    * <= 4096. */
   int d_cq;
+  /* Storage of the latent cache rows: MLA_KV_NATIVE (the context dtype,
+   * (d_latent + d_rope) elements per row) or MLA_KV_FP8 (bf16 contexts at
+   * DeepSeek-V2 widths only).  An FP8 row is 656 bytes:
+   *   bytes   0..511  the 512 latent values c^KV as E4M3 codes (OCP OFP8
+   *                   E4M3: bias 7, 3 mantissa bits, largest value 448),
+   *   bytes 512..639  the 64 RoPE-key values k^R as bf16, divided by s,
+   *   bytes 640..643  s (fp32), bytes 644..655 zero,
+   * standing for [s * E4M3(code_i) ; s * stored_j].  s = amax / 448 with
+   * amax = max |c_i| of the row as produced in bf16 (s = 1 for a zero
+   * row), code_i = E4M3(c_i * (448 / amax)) rounded to nearest-even with
+   * saturation, each quotient and product rounded to fp32.  The pages name
+   * FP8 for the attention GEMMs of the forward pass (tuntang.top
+   * "DeepSeek 系列模型技术深度解读", "FP8 混合精度训练") but give no scaling
+   * scheme for a cache; this per-row one lets the score contraction run on
+   * the E4M3 codes with a single accumulator. */
+  int kv_dtype;
 } mla_config;
+
+enum { MLA_KV_NATIVE = 0, MLA_KV_FP8 = 1 };
+#define MLA_FP8_ROW_BYTES 656
 
 /* Device pointers to the projection matrices (layouts above).  The last
  * three (query path, mla_layer_step) are read only when d_cq > 0:
@@ -123,9 +142,11 @@ mla_status mla_destroy(mla_ctx* ctx);
  *               < max_position).
  *   block_table device int32 [batch, max_pages]: physical page of each
  *               logical page of each sequence.
- *   cache       device, [num_pages*page_size, d_latent+d_rope], the pool.
+ *   cache       device, [num_pages*page_size, d_latent+d_rope], the pool
+ *               (rows of MLA_FP8_ROW_BYTES bytes with MLA_KV_FP8).
  * Writes row [W^DKV h ; RoPE_pos(W^KR h)] (fp32 accumulation, rounded once
- * to the context dtype) to pool row
+ * to the context dtype; with MLA_KV_FP8 rounded to bf16, then quantised as
+ * the kv_dtype comment states) to pool row
  *   block_table[b][pos / page_size] * page_size + pos % page_size.
  * Rows of other tokens are untouched.  A page id outside [0, num_pages) or
  * a position out of range skips that token and sets MLA_ERR_DEVICE_INDEX.
@@ -207,7 +228,8 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
  * explicit form's buffers: the gathered rows, K^C and V of every row of
  * the batch (batch·max_pages·page_size rows of 1152 + 2·32768 bytes), the
  * rotated queries and the per-head outputs.  MLA_ERR_UNSUPPORTED for
- * MLA_FORM_EXPLICIT on an fp32 context, MLA_ERR_INVALID_ARG for it past
+ * MLA_FORM_EXPLICIT on an fp32 context or an FP8 cache (the explicit form
+ * reads bf16 rows), MLA_ERR_INVALID_ARG for it past
  * the row bound.  Device-side index errors are reported as for
  * mla_append_decode. */
 enum { MLA_FORM_AUTO = 0, MLA_FORM_EXPLICIT = 1, MLA_FORM_ABSORBED = 2 };
@@ -224,7 +246,8 @@ size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T,
  * token (absorbed query, combine, W^UV).  With S = max_pages·page_size keys
  * per sequence: the explicit form for prompts on an empty cache from a few
  * dozen tokens up, the absorbed form for decode and for short chunks after
- * a long prefix (below about 460 tokens after 12288).  fp32 contexts, and calls whose batch·max_pages·page_size exceeds
+ * a long prefix (below about 460 tokens after 12288).  fp32 contexts, FP8
+ * caches, and calls whose batch·max_pages·page_size exceeds
  * 2^18 rows, always get MLA_FORM_ABSORBED. */
 int mla_prefill_form(const mla_ctx* ctx, int batch, int T, int max_pages);
 

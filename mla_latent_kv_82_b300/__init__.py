@@ -24,6 +24,9 @@ MLA_ERR_TIMEOUT = 5
 MLA_ERR_DEVICE_INDEX = 6
 MLA_BF16 = 0
 MLA_FP32 = 1
+MLA_KV_NATIVE = 0
+MLA_KV_FP8 = 1
+MLA_FP8_ROW_BYTES = 656
 MLA_FORM_AUTO = 0
 MLA_FORM_EXPLICIT = 1
 MLA_FORM_ABSORBED = 2
@@ -43,7 +46,7 @@ class mla_config(ctypes.Structure):
         ("d_v", ctypes.c_int), ("d_latent", ctypes.c_int), ("d_rope", ctypes.c_int),
         ("page_size", ctypes.c_int), ("max_position", ctypes.c_int),
         ("softmax_scale", ctypes.c_float), ("rope_base", ctypes.c_float),
-        ("dtype", ctypes.c_int), ("d_cq", ctypes.c_int),
+        ("dtype", ctypes.c_int), ("d_cq", ctypes.c_int), ("kv_dtype", ctypes.c_int),
     ]
 
 
@@ -224,7 +227,7 @@ class MLA:
     """Owns a context over torch-held weights; passes tensor pointers through."""
 
     def __init__(self, dims, weights: dict, dtype: str, max_position: int, device: int = 0,
-                 softmax_scale: float | None = None):
+                 softmax_scale: float | None = None, kv: str = "native"):
         import torch  # noqa: F401  (tensors only provide pointers and streams)
         self.dims = dims
         self.weights = {k: v.contiguous() for k, v in weights.items()}
@@ -233,7 +236,9 @@ class MLA:
                          dims.d_rope, dims.page_size, max_position,
                          softmax_scale if softmax_scale is not None else dims.softmax_scale,
                          dims.rope_base, MLA_BF16 if dtype == "bf16" else MLA_FP32,
-                         getattr(dims, "d_cq", 0))
+                         getattr(dims, "d_cq", 0),
+                         MLA_KV_FP8 if kv == "fp8" else MLA_KV_NATIVE)
+        self.kv = kv
         names = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o", "w_dq", "w_uq", "w_qr")
         w = mla_weights(*(self.weights[k].data_ptr() if k in self.weights else None
                           for k in names))

@@ -47,6 +47,8 @@ mla_status validate_config(const mla_config* c) {
   } else {
     return MLA_ERR_INVALID_ARG;
   }
+  if (c->kv_dtype != MLA_KV_NATIVE && c->kv_dtype != MLA_KV_FP8) return MLA_ERR_INVALID_ARG;
+  if (c->kv_dtype == MLA_KV_FP8 && c->dtype != MLA_BF16) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }
 
@@ -335,7 +337,7 @@ mla_status mla_layer_step(mla_ctx* ctx, const void* h, const int32_t* positions,
 constexpr long long kExplicitRows = 1LL << 18;
 
 static bool explicit_fits(const mla_ctx* ctx, int batch, int max_pages) {
-  return ctx->cfg.dtype == MLA_BF16 &&
+  return ctx->cfg.dtype == MLA_BF16 && ctx->cfg.kv_dtype == MLA_KV_NATIVE &&
          (long long)batch * max_pages * ctx->cfg.page_size <= kExplicitRows;
 }
 
@@ -386,7 +388,8 @@ mla_status mla_prefill(mla_ctx* ctx, const void* h, const int32_t* positions, co
     return MLA_ERR_INVALID_ARG;
   if (form < MLA_FORM_AUTO || form > MLA_FORM_ABSORBED) return MLA_ERR_INVALID_ARG;
   const bool bf = ctx->cfg.dtype == MLA_BF16;
-  if (!bf && form == MLA_FORM_EXPLICIT) return MLA_ERR_UNSUPPORTED;
+  if ((!bf || ctx->cfg.kv_dtype != MLA_KV_NATIVE) && form == MLA_FORM_EXPLICIT)
+    return MLA_ERR_UNSUPPORTED;
   if (form == MLA_FORM_EXPLICIT && !explicit_fits(ctx, batch, max_pages))
     return MLA_ERR_INVALID_ARG;
   const size_t a = bf ? 16 : 4;

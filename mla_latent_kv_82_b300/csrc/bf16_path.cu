@@ -254,6 +254,11 @@ bool bf16_setup(mla_ctx* ctx) {
   }
   if (!ok) return false;
   if (!sv_setup(ctx)) return false;
+  if (kv_fp8(ctx) &&
+      cudaMalloc(&ctx->stage, (size_t)kStageRows * kRow * sizeof(__nv_bfloat16)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
   if (cudaMalloc(&ctx->append_partials, kAppendPartialBytes) != cudaSuccess ||
       cudaMalloc(&ctx->counters, kCounters * sizeof(int)) != cudaSuccess ||
       cudaMemset(ctx->counters, 0, kCounters * sizeof(int)) != cudaSuccess) {
@@ -264,6 +269,8 @@ bool bf16_setup(mla_ctx* ctx) {
 }
 
 void bf16_teardown(mla_ctx* ctx) {
+  if (ctx->stage) cudaFree(ctx->stage);
+  ctx->stage = nullptr;
   if (ctx->append_partials) cudaFree(ctx->append_partials);
   if (ctx->counters) cudaFree(ctx->counters);
   ctx->append_partials = nullptr;
@@ -309,6 +316,28 @@ static bool append_plan(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T, cons
 bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           const int32_t* pos, const int32_t* bt, int max_pages,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
+  if (kv_fp8(ctx)) {
+    // bf16 rows of up to kStageRows tokens at a time into the staging
+    // buffer, then quantised into the pool
+    const int M = B * T, D = ctx->cfg.d_model;
+    for (int m0 = 0; m0 < M; m0 += kStageRows) {
+      const int mc = std::min(kStageRows, M - m0);
+      WgPlan p;
+      if (!append_plan(ctx, h + (size_t)m0 * D, 1, mc, pos + m0, bt, max_pages, ctx->stage,
+                       num_pages, p))
+        return false;
+      p.args.stage_rows = 1;
+      prof_mark(ctx, st, "compress_append");
+      ctx->launches += 1;
+      if (!check(wgemm_launch(p, WG_APPEND, false, st, true))) return false;
+      if (!f8_prepare(ctx, ctx->stage, mc, m0, pos, bt, T, max_pages,
+                      reinterpret_cast<uint8_t*>(cache), num_pages, nullptr, 0, nullptr, st)) {
+        cudaGetLastError();
+        return false;
+      }
+    }
+    return true;
+  }
   WgPlan p;
   if (!append_plan(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, p)) return false;
   prof_mark(ctx, st, "compress_append");
@@ -375,7 +404,20 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     }
   }
   // ---- split-KV attention over the latent cache
-  if (!sv_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) return false;
+  if (kv_fp8(ctx)) {
+    // the appended rows (staged in bf16) into the FP8 pool, the query images
+    // into FP8 images, then the attention on E4M3 operands
+    uint8_t* q8 = reinterpret_cast<uint8_t*>(ws + L.q8);
+    uint8_t* cache8 = reinterpret_cast<uint8_t*>(const_cast<__nv_bfloat16*>(cache));
+    if (!f8_prepare(ctx, ctx->stage, append ? M : 0, 0, append ? append->args.pos : nullptr, bt,
+                    T, max_pages, cache8, num_pages, qimg, M, q8, st) ||
+        !f8_attend(ctx, q8, cache8, num_pages, bt, max_pages, B, T, ws, L, st)) {
+      cudaGetLastError();
+      return false;
+    }
+  } else if (!sv_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) {
+    return false;
+  }
   // ---- log-sum-exp combine -> o_lat (bf16)
   {
     prof_mark(ctx, st, "combine");
@@ -567,8 +609,16 @@ bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos
                         const __nv_bfloat16* q, __nv_bfloat16* cache, int num_pages,
                         const int32_t* bt, int max_pages, const int32_t* seq_lens, int B, int T,
                         __nv_bfloat16* out, char* ws, const WsLayout& L, cudaStream_t st) {
+  if (kv_fp8(ctx) && B * T > kStageRows) {
+    // more rows than one staging pass: append first, then decode
+    return bf16_compress_append(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, st) &&
+           bf16_decode(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st);
+  }
   WgPlan p;
-  if (!append_plan(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, p)) return false;
+  if (!append_plan(ctx, h, B, T, pos, bt, max_pages, kv_fp8(ctx) ? ctx->stage : cache, num_pages,
+                   p))
+    return false;
+  p.args.stage_rows = kv_fp8(ctx) ? 1 : 0;
   return bf16_decode(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st, &p);
 }
 

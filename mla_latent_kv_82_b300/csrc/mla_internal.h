@@ -25,6 +25,8 @@ struct mla_ctx {
   CUtensorMap tm_wuk_rows;              // W^UK with 128-row boxes (K^C = W^UK c)
   CUtensorMap tm_wdq, tm_wuq, tm_wqr;   // query path (d_cq > 0)
   float* append_partials = nullptr;   // kAppendPartialBytes
+  // FP8 cache: bf16 rows [kStageRows, 576] of an append before quantisation
+  __nv_bfloat16* stage = nullptr;
   int* counters = nullptr;            // kCounters, zero between launches
   // attention clusters that fit on the device at once: [0] two-CTA clusters
   // (odd T), [1] four-CTA clusters (even T)
@@ -39,6 +41,9 @@ struct mla_ctx {
 namespace mla {
 
 constexpr size_t kAppendPartialBytes = 8u << 20;
+constexpr int kStageRows = 4096;        // tokens per FP8 append pass
+constexpr int kF8Row = 656;             // bytes of an FP8 cache row
+constexpr int kQ8Bytes = 82432;         // FP8 query image of one token
 constexpr int kCounters = 65536;
 
 // Byte layout of the decode workspace (all offsets 256-byte aligned).
@@ -55,6 +60,7 @@ struct WsLayout {
   size_t wg_part;  // fp32 split-K partials of the projections
   size_t c_q;      // query path (d_cq > 0): dtype [batch*T, d_cq]
   size_t q_in;     // query path: dtype [batch*T, n_heads, d_nope + d_rope]
+  size_t q8;       // FP8 cache: [batch*T] FP8 query images of kQ8Bytes
   size_t total;
 };
 
@@ -114,7 +120,7 @@ bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int 
                         const __nv_bfloat16* x, int M, int x_cols, __nv_bfloat16* out,
                         int ld_out, float* part, cudaStream_t st, const char* name);
 
-// Query path of mla_layer_step:// Query path of mla_layer_step: q = [W^UQ W^DQ h ; W^QR h] per head into
+// Query path of mla_layer_step: q = [W^UQ W^DQ h ; W^QR h] per head into
 // the workspace's q_in (layout of mla_decode's q).
 bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsLayout& L,
                 cudaStream_t st);
@@ -132,6 +138,18 @@ bool sv_attend(mla_ctx* ctx, const __nv_bfloat16* qimg, const __nv_bfloat16* cac
                const WsLayout& L, cudaStream_t st);
 // Fills ctx->sv_clusters (at context creation).
 bool sv_setup(mla_ctx* ctx);
+// FP8 cache (attend_f8.cu).  f8_prepare quantises `rows` staged bf16 rows
+// (tokens m0.. of the batch; none when rows == 0) into the pool and the M_q
+// bf16 query images into FP8 query images, in one launch.
+bool f8_prepare(mla_ctx* ctx, const __nv_bfloat16* stage, int rows, int m0, const int32_t* pos,
+                const int32_t* bt, int T, int max_pages, uint8_t* cache8, int num_pages,
+                const __nv_bfloat16* qimg, int M_q, uint8_t* q8img, cudaStream_t st);
+// Split-KV attention over the FP8 pool: two CTAs (latent halves) per
+// (KV split, query token).
+bool f8_attend(mla_ctx* ctx, const uint8_t* q8img, const uint8_t* cache8, int num_pages,
+               const int32_t* bt, int max_pages, int B, int T, char* ws, const WsLayout& L,
+               cudaStream_t st);
+inline bool kv_fp8(const mla_ctx* ctx) { return ctx->cfg.kv_dtype == MLA_KV_FP8; }
 
 void launch_selftest_wait(const mla_ctx* ctx, int spin_limit, cudaStream_t st);
 

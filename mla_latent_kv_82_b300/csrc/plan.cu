@@ -57,7 +57,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static int choose_splits(const mla_ctx* ctx, int B, int T, int max_pages) {
   const long long pages_bound = (long long)B * max_pages;
   int G;
-  if (ctx->cfg.dtype == MLA_BF16) {
+  if (kv_fp8(ctx)) {
+    // two CTAs (latent halves) per (split, query token), one per SM
+    G = ctx->num_sms / (2 * T);
+  } else if (ctx->cfg.dtype == MLA_BF16) {
     // one cluster of two CTAs per (split, query token) for odd T, of four
     // per (split, token pair) for even T, one CTA per SM, all resident at once
     G = ctx->num_sms / (2 * T);
@@ -97,6 +100,7 @@ WsLayout workspace_layout(const mla_ctx* ctx, int B, int T, int max_pages) {
     L.c_q = take(es * M * c.d_cq);
     L.q_in = take(es * M * c.n_heads * (c.d_nope + c.d_rope));
   }
+  if (kv_fp8(ctx)) L.q8 = take((size_t)kQ8Bytes * M);
   L.total = off;
   return L;
 }

@@ -132,6 +132,28 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4 with E4M3 A and B and
+// an fp32 accumulator (A and B formats 0 = E4M3 in the f8f6f4 encoding).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                                 // D format: f32
+         | (0u << 7)                               // A format: E4M3
+         | (0u << 10)                              // B format: E4M3
+         | ((uint32_t)(N >> 3) << 17)              // N / 8
+         | ((uint32_t)(M >> 4) << 24);             // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem] on E4M3 operands (K = 32 per instruction,
+// 32 bytes of each K-major row).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]; A is M rows (lanes) x K bf16 packed two per
 // 32-bit column (element 2j in the low half of column j).
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,

@@ -64,4 +64,18 @@ bool make_tmap_pool_slabs(CUtensorMap* tm, const void* base, uint64_t rows, uint
   return encode_pool(tm, base, 4, dims, strides, box);
 }
 
+bool make_tmap_u8_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t row_bytes,
+                     uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mla

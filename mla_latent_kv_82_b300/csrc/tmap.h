@@ -25,4 +25,11 @@ bool make_tmap_pool_blocks(CUtensorMap* tm, const void* base, uint64_t rows, uin
                            uint32_t nb);
 bool make_tmap_pool_slabs(CUtensorMap* tm, const void* base, uint64_t rows, uint32_t nb);
 
+// Tiled map of a byte matrix [rows, row_bytes] (row stride row_bytes, a
+// multiple of 16), box = box_rows x box_bytes; swizzle128 selects the
+// 128-byte swizzle (box_bytes must then be 128), else no swizzle (box_bytes a
+// multiple of 16).  Zero fill out of bounds.
+bool make_tmap_u8_2d(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t row_bytes,
+                     uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
+
 }  // namespace mla

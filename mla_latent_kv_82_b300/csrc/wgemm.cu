@@ -270,6 +270,8 @@ __device__ __forceinline__ void wgemm_body(const CUtensorMap& tmA, const CUtenso
             dst = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(a.qimg) +
                                                    (size_t)t * kQImgBytes +
                                                    qimg_off(head, tile * 128 + ch * 8));
+          } else if (a.stage_rows) {   // WG_APPEND into a staging buffer, row t
+            dst = a.cache + (size_t)t * kRow + tile * 128 + ch * 8;
           } else {   // WG_APPEND
             const int pos = a.pos[t];
             const int b = t / a.T;

@@ -32,6 +32,7 @@ struct WgArgs {
   const int32_t* pos;
   const int32_t* bt;
   int max_pages, num_pages, T, max_position, append_rope_tile;
+  int stage_rows;        // write token t's row to cache + t * 576 (no paging)
   const float2* rope_cs;
   // WG_QIMG: absorbed-query image per token; RoPE of q^R by tile-0 CTAs at
   // the position plan_len(seq_lens) - T + t; with do_plan, the epilogue

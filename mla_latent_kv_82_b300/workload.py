@@ -23,7 +23,8 @@ Q_NAMES = ("w_dq", "w_uq", "w_qr")
 
 class DeviceState:
     def __init__(self, wl, device: int = 0, prefill: bool = True, chunk: int = 32768,
-                 sentinel: float | None = None, block_table=None, query_path: bool = False):
+                 sentinel: float | None = None, block_table=None, query_path: bool = False,
+                 kv: str = "native"):
         self.wl = wl
         self.dev = torch.device("cuda", device)
         d = wl.dims
@@ -31,13 +32,18 @@ class DeviceState:
         names = W_NAMES + (Q_NAMES if query_path else ())
         self.weights = {n: wl.weight(n, device=self.dev) for n in names}
         ctx_dims = d if query_path else dataclasses.replace(d, d_cq=0)
+        self.kv = kv
         self.mla = MLA(ctx_dims, self.weights, wl.dtype, max_position=max(wl.seq_lens),
-                       device=device)
+                       device=device, kv=kv)
         bt = wl.block_table() if block_table is None else block_table
         self.bt = torch.as_tensor(bt, dtype=torch.int32, device=self.dev).contiguous()
         self.num_pages = int(self.bt.max().item()) + 1
         rows = self.num_pages * d.page_size
-        if sentinel is None:
+        if kv == "fp8":
+            # FP8 rows of MLA_FP8_ROW_BYTES bytes; the sentinel is a byte value
+            self.cache = torch.full((rows, 656), 0 if sentinel is None else int(sentinel),
+                                    dtype=torch.uint8, device=self.dev)
+        elif sentinel is None:
             self.cache = torch.empty((rows, d.row_width), dtype=dt, device=self.dev)
         else:
             self.cache = torch.full((rows, d.row_width), sentinel, dtype=dt, device=self.dev)
