@@ -27,11 +27,11 @@
 // (per tile: four latent blocks [128 keys][128 codes], then the RoPE block
 // [128 keys][64 bf16]), two buffers of a tile's row scales, and this half's
 // values of the tile widened to bf16 (64 KB).
-// Roles (256 threads): warp 0 TMA producer; warp 1 MMA issuer (S, then the
-// previous tile's PV) and TMEM owner; warps 2-5 softmax and epilogue
-// (thread = head); warps 6-7 load this half's codes of each tile straight
-// from the pool into registers (ahead of time) and, once the previous PV has
-// read the value buffer, widen them into it.
+// Roles (256 threads): warp 0 TMA producer; warp 1 score-MMA issuer and
+// TMEM owner; warps 2-5 softmax and epilogue (thread = head); warps 6-7 load
+// this half's codes of each tile straight from the pool into registers (a
+// tile ahead), widen them into the value buffer once the previous PV has
+// read it, and issue the tile's value MMAs.
 // Every wait is bounded; on a timeout the CTA records MLA_ERR_TIMEOUT,
 // drains its own copies and frees TMEM.
 #include "attend_common.cuh"
@@ -65,13 +65,13 @@ enum : int {
   kSF = 8,    // [2] S of tiles of that parity done
   kPF = 10,   // [2] P' written (4 softmax warps)
   kPD = 12,   // [2] PV of tiles of that parity done
-  kVF = 14,   // [2] values of the tile widened (converters)
+  // 14, 15 unused
   kCF = 16,   // [2] row scales of the tile loaded
   kCE = 18,   // [2] row scales read (4 softmax warps)
   kQF = 20,   // query image loaded
   kQE = 21,   // query image consumed: last S commit + 4 softmax warps (scales read)
   kOF = 22,   // epilogue read O (4 softmax warps)
-  kDR = 23,   // the MMA issuer's last MMAs done
+  kDR = 23,   // the last score MMAs and the last value MMAs done
   kSlot = 24  // tmem slot, abort flag, converter failure flag
 };
 
@@ -139,14 +139,13 @@ attend_f8_kernel(const __grid_constant__ CUtensorMap tmB,   // pool, box {128 B,
       mbar_init(&bar[kSF + i], 1);
       mbar_init(&bar[kPF + i], 4);
       mbar_init(&bar[kPD + i], 1);
-      mbar_init(&bar[kVF + i], 1);
       mbar_init(&bar[kCF + i], 1);
       mbar_init(&bar[kCE + i], 4);
     }
     mbar_init(&bar[kQF], 1);
     mbar_init(&bar[kQE], 5);
     mbar_init(&bar[kOF], 4);
-    mbar_init(&bar[kDR], 1);
+    mbar_init(&bar[kDR], 2);
     *abort_flag = 0;
     *conv_fail = 0;
     tc::fence_barrier_init();
@@ -228,92 +227,58 @@ attend_f8_kernel(const __grid_constant__ CUtensorMap tmB,   // pool, box {128 B,
     }
     if (!ok) *abort_flag = 1;
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    // Per tile: S(g) on the four latent blocks and the RoPE block, then
-    // PV(g - 1), so that S(g) overlaps the softmax of tile g - 1.
+    // ---------------------------------------------------------- score MMA issuer
+    // Per tile S(g) on the four latent blocks and the RoPE block; the value
+    // MMAs are issued by the converters once they have filled the value
+    // buffer, so that neither waits behind the other.
     const bool leader = tc::elect_one();
     constexpr uint32_t idS8 = tc::idesc_e4m3(128, kTile);
     constexpr uint32_t idSR = tc::idesc_bf16(128, kTile, false, false);
-    constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
     const uint64_t dQ = tc::sdesc(sQ, 16, 1024);
     const uint64_t dR = tc::sdesc(sR, 16, 1024);
-    const uint64_t dV = tc::sdesc(smem_u32(smem + kOffV8), 16384, 1024);   // MN-major values
     SegIter it;
     it.init(&a, c, t);
-    int sb, p0, p1, slot, k = 0, g0 = 0;
+    int sb, p0, p1, slot, k = 0, g = 0;
     bool ok = true;
     while (ok && it.next(&sb, &p0, &p1, &slot)) {
       const int n = ntiles_of(p0, p1);
       if (n == 0) continue;
       if (!warp_wait(&bar[kQF], k & 1, a.status, 124)) { ok = false; break; }
-      for (int i = 0; ok && i <= n; ++i) {
-        const int gs = g0 + i, gv = gs - 1;
-        if (i < n) {
-          // S(gs) reuses the columns P(gs - 2) was read from
-          if (gs >= 2 &&
-              !warp_wait(&bar[kPD + (gs & 1)], ((gs - 2) >> 1) & 1, a.status, 125)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dcol = tmem + kColS + (gs & 1) * kTile;
-          for (int kb = 0; kb < 5; ++kb) {
-            const int nr = 5 * gs + kb, s = nr % kF8Ring;
-            if (!warp_wait(&bar[kF + s], (nr / kF8Ring) & 1, a.status, 126)) { ok = false; break; }
-            tc::fence_after_sync();
-            if (leader) {
-              const uint64_t b = dR + ((s * kF8Stage) >> 4);
-              if (kb < 4) {
-                const uint64_t q = dQ + ((kb * 16384) >> 4);
-                tc::mma_ss_f8(dcol, q, b, idS8, kb > 0 ? 1u : 0u);
-                tc::mma_ss_f8(dcol, q + 2, b + 2, idS8, 1u);
-                tc::mma_ss_f8(dcol, q + 4, b + 4, idS8, 1u);
-                tc::mma_ss_f8(dcol, q + 6, b + 6, idS8, 1u);
-              } else {
-                const uint64_t q = dQ + (kQ8Rope >> 4);
-                tc::mma_ss(dcol, q, b, idSR, 1u);
-                tc::mma_ss(dcol, q + 2, b + 2, idSR, 1u);
-                tc::mma_ss(dcol, q + 4, b + 4, idSR, 1u);
-                tc::mma_ss(dcol, q + 6, b + 6, idSR, 1u);
-              }
-              tc::mma_commit(smem_u32(&bar[kE + s]));
-            }
-          }
-          if (!ok) break;
-          if (leader) {
-            tc::mma_commit(smem_u32(&bar[kSF + (gs & 1)]));
-            if (i == n - 1) tc::mma_commit(smem_u32(&bar[kQE]));
-          }
+      for (int i = 0; ok && i < n; ++i, ++g) {
+        // S(g) reuses the columns P(g - 2) was read from
+        if (g >= 2 && !warp_wait(&bar[kPD + (g & 1)], ((g - 2) >> 1) & 1, a.status, 125)) {
+          ok = false;
+          break;
         }
-        if (i >= 1) {
-          // PV(gv); the first of a segment overwrites O once the previous
-          // segment's epilogue has read it
-          if (i == 1 && k > 0 && !warp_wait(&bar[kOF], (k - 1) & 1, a.status, 127)) {
-            ok = false;
-            break;
-          }
-          if (!warp_wait(&bar[kPF + (gv & 1)], (gv >> 1) & 1, a.status, 128) ||
-              !warp_wait(&bar[kVF + (gv & 1)], (gv >> 1) & 1, a.status, 129)) {
-            ok = false;
-            break;
-          }
-          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        const uint32_t dcol = tmem + kColS + (g & 1) * kTile;
+        for (int kb = 0; kb < 5; ++kb) {
+          const int nr = 5 * g + kb, s = nr % kF8Ring;
+          if (!warp_wait(&bar[kF + s], (nr / kF8Ring) & 1, a.status, 126)) { ok = false; break; }
           tc::fence_after_sync();
           if (leader) {
-            const uint32_t pcol = tmem + kColS + (gv & 1) * kTile;
-            const uint32_t acc = i > 1 ? 1u : 0u;
-            tc::mma_ts(tmem, pcol, dV, idO, acc);
-            tc::mma_ts(tmem, pcol + 8, dV + (2048 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 16, dV + (4096 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 24, dV + (6144 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 32, dV + (8192 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 40, dV + (10240 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 48, dV + (12288 >> 4), idO, 1u);
-            tc::mma_ts(tmem, pcol + 56, dV + (14336 >> 4), idO, 1u);
-            tc::mma_commit(smem_u32(&bar[kPD + (gv & 1)]));
+            const uint64_t b = dR + ((s * kF8Stage) >> 4);
+            if (kb < 4) {
+              const uint64_t q = dQ + ((kb * 16384) >> 4);
+              tc::mma_ss_f8(dcol, q, b, idS8, kb > 0 ? 1u : 0u);
+              tc::mma_ss_f8(dcol, q + 2, b + 2, idS8, 1u);
+              tc::mma_ss_f8(dcol, q + 4, b + 4, idS8, 1u);
+              tc::mma_ss_f8(dcol, q + 6, b + 6, idS8, 1u);
+            } else {
+              const uint64_t q = dQ + (kQ8Rope >> 4);
+              tc::mma_ss(dcol, q, b, idSR, 1u);
+              tc::mma_ss(dcol, q + 2, b + 2, idSR, 1u);
+              tc::mma_ss(dcol, q + 4, b + 4, idSR, 1u);
+              tc::mma_ss(dcol, q + 6, b + 6, idSR, 1u);
+            }
+            tc::mma_commit(smem_u32(&bar[kE + s]));
           }
         }
+        if (!ok) break;
+        if (leader) {
+          tc::mma_commit(smem_u32(&bar[kSF + (g & 1)]));
+          if (i == n - 1) tc::mma_commit(smem_u32(&bar[kQE]));
+        }
       }
-      g0 += n;
       ++k;
     }
     if (!ok) *abort_flag = 1;
@@ -322,66 +287,131 @@ attend_f8_kernel(const __grid_constant__ CUtensorMap tmB,   // pool, box {128 B,
     // ---------------------------------------------------------- converters
     // Tile g's codes of this half (latent blocks vb0, vb0 + 1: 256 bytes of
     // each key's row) come straight from the pool into registers, 32
-    // 16-byte pieces per thread, before waiting for PV(g - 1); then they are
-    // widened to bf16 into the value buffer ([128 keys][256 columns] as four
-    // 128-byte-swizzled blocks of 64 columns).  Keys past the visible end
-    // become zeros, so that 0 * (NaN or Inf) never reaches the accumulator.
+    // 16-byte pieces per thread; once PV(g - 1) has read the value buffer
+    // they are widened to bf16 into it ([128 keys][256 columns] as four
+    // 128-byte-swizzled blocks of 64 columns), and each register is refilled
+    // with the next tile's piece as soon as it is widened, so that a tile's
+    // loads are in flight while the previous tile is consumed.  Keys past
+    // the visible end become zeros, so that 0 * (NaN or Inf) never reaches
+    // the accumulator.
     const int ct = threadIdx.x - 192;   // 0..63
     const uint8_t* pool = reinterpret_cast<const uint8_t*>(a.cache);
+    // tile walk: the (sequence, first key, visible end) of each tile
     SegIter it;
     it.init(&a, c, t);
-    int sb, p0, p1, slot, g = 0;
+    int sb = 0, p0 = 0, p1 = 0, slot = 0, i = 0, n = 0;
+    auto next_tile = [&](int* tsb, int* tts, int* tp1, bool* tfirst) -> bool {
+      while (i >= n) {
+        if (!it.next(&sb, &p0, &p1, &slot)) return false;
+        n = ntiles_of(p0, p1);
+        i = 0;
+      }
+      *tsb = sb;
+      *tts = p0 + i * kTile;
+      *tp1 = p1;
+      *tfirst = i == 0;
+      ++i;
+      return true;
+    };
+    uint4 wv[32];
+    // issue the loads of one tile (zeros past its visible end)
+    auto load_tile = [&](int lsb, int lts, int lp1) {
+      TilePages tp;
+      tp.load(a, lsb, lts, lp1);
+      const int y0 = tp.row(a, 0, lsb, oob_row), y1 = tp.row(a, 1, lsb, oob_row);
+      const int vis = min(kTile, lp1 - lts);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int task = ct + 64 * j;
+        const int kl = task >> 10, r = (task >> 3) & 127, ch = task & 7;
+        wv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < vis)
+          wv[j] = tc::ld_nc_v4(pool + (size_t)((r < kPage ? y0 : y1 - kPage) + r) * kF8Row +
+                               (vb0 + kl) * 128 + ch * 16);
+      }
+    };
+    int csb, cts, cp1;
+    bool cfirst;
+    bool have = next_tile(&csb, &cts, &cp1, &cfirst);
+    if (have) load_tile(csb, cts, cp1);
     bool ok = true;
     uint8_t* vbuf = smem + kOffV8;
-    while (ok && it.next(&sb, &p0, &p1, &slot)) {
-      const int n = ntiles_of(p0, p1);
-      for (int i = 0; i < n; ++i, ++g) {
-        const int ts = p0 + i * kTile;
-        const int vis = min(kTile, p1 - ts);
+    constexpr uint32_t idO = tc::idesc_bf16(128, 256, false, true);
+    const uint64_t dV = tc::sdesc(smem_u32(vbuf), 16384, 1024);   // MN-major values
+    int kseg = -1;   // segment of the current tile (segments with tiles only)
+    for (int g = 0; have; ++g) {
+      if (cfirst) ++kseg;
+      int nsb, nts, np1;
+      bool nfirst = false;
+      const bool more = next_tile(&nsb, &nts, &np1, &nfirst);
+      bool w = true;
+      if (g >= 1)
+        w = bar_wait<false>(&bar[kPD + ((g - 1) & 1)], ((g - 1) >> 1) & 1, a.status, 130);
+      if (!w || *abort_flag) *conv_fail = 1;
+      tc::named_sync(2, 64);
+      if (*conv_fail) { ok = false; break; }   // read after the barrier: the same for all
+      // the next tile's rows, validated as the producer validates them
+      int ny0 = 0, ny1 = 0, nvis = 0;
+      if (more) {
         TilePages tp;
-        tp.load(a, sb, ts, p1);
-        const int y0 = tp.row(a, 0, sb, oob_row), y1 = tp.row(a, 1, sb, oob_row);
-        uint4 wv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int task = ct + 64 * j;
-          const int kl = task >> 10, r = (task >> 3) & 127, ch = task & 7;
-          wv[j] = make_uint4(0u, 0u, 0u, 0u);
-          if (r < vis)
-            wv[j] = tc::ld_nc_v4(pool + (size_t)((r < kPage ? y0 : y1 - kPage) + r) * kF8Row +
-                                 (vb0 + kl) * 128 + ch * 16);
-        }
-        bool w = true;
-        if (g >= 1)
-          w = bar_wait<false>(&bar[kPD + ((g - 1) & 1)], ((g - 1) >> 1) & 1, a.status, 130);
-        if (!w || *abort_flag) *conv_fail = 1;
-        tc::named_sync(2, 64);
-        if (*conv_fail) { ok = false; break; }   // read after the barrier: the same for all
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int task = ct + 64 * j;
-          const int kl = task >> 10, r = (task >> 3) & 127, ch = task & 7;
-          uint4 lo, hi;
-          lo.x = e4m3x2_bf16x2(__byte_perm(wv[j].x, 0u, 0x4140));
-          lo.y = e4m3x2_bf16x2(__byte_perm(wv[j].x, 0u, 0x4342));
-          lo.z = e4m3x2_bf16x2(__byte_perm(wv[j].y, 0u, 0x4140));
-          lo.w = e4m3x2_bf16x2(__byte_perm(wv[j].y, 0u, 0x4342));
-          hi.x = e4m3x2_bf16x2(__byte_perm(wv[j].z, 0u, 0x4140));
-          hi.y = e4m3x2_bf16x2(__byte_perm(wv[j].z, 0u, 0x4342));
-          hi.z = e4m3x2_bf16x2(__byte_perm(wv[j].w, 0u, 0x4140));
-          hi.w = e4m3x2_bf16x2(__byte_perm(wv[j].w, 0u, 0x4342));
-          const int col = kl * 128 + ch * 16;           // column within this half
-          const int vb = col >> 6, cc = (col & 63) >> 3;
-          uint8_t* dst = vbuf + vb * 16384 + r * 128;
-          *reinterpret_cast<uint4*>(dst + ((cc ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((cc + 1) ^ (r & 7)) << 4)) = hi;
-        }
-        tc::fence_async_smem();
-        tc::named_sync(2, 64);
-        if (ct == 0) tc::mbar_arrive(smem_u32(&bar[kVF + (g & 1)]));
+        tp.load(a, nsb, nts, np1);
+        ny0 = tp.row(a, 0, nsb, oob_row);
+        ny1 = tp.row(a, 1, nsb, oob_row);
+        nvis = min(kTile, np1 - nts);
       }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int task = ct + 64 * j;
+        const int kl = task >> 10, r = (task >> 3) & 127, ch = task & 7;
+        uint4 lo, hi;
+        lo.x = e4m3x2_bf16x2(__byte_perm(wv[j].x, 0u, 0x4140));
+        lo.y = e4m3x2_bf16x2(__byte_perm(wv[j].x, 0u, 0x4342));
+        lo.z = e4m3x2_bf16x2(__byte_perm(wv[j].y, 0u, 0x4140));
+        lo.w = e4m3x2_bf16x2(__byte_perm(wv[j].y, 0u, 0x4342));
+        hi.x = e4m3x2_bf16x2(__byte_perm(wv[j].z, 0u, 0x4140));
+        hi.y = e4m3x2_bf16x2(__byte_perm(wv[j].z, 0u, 0x4342));
+        hi.z = e4m3x2_bf16x2(__byte_perm(wv[j].w, 0u, 0x4140));
+        hi.w = e4m3x2_bf16x2(__byte_perm(wv[j].w, 0u, 0x4342));
+        const int col = kl * 128 + ch * 16;           // column within this half
+        const int vb = col >> 6, cc = (col & 63) >> 3;
+        uint8_t* dst = vbuf + vb * 16384 + r * 128;
+        *reinterpret_cast<uint4*>(dst + ((cc ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + (((cc + 1) ^ (r & 7)) << 4)) = hi;
+        // refill with the next tile's piece
+        wv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (more && r < nvis)
+          wv[j] = tc::ld_nc_v4(pool + (size_t)((r < kPage ? ny0 : ny1 - kPage) + r) * kF8Row +
+                               (vb0 + kl) * 128 + ch * 16);
+      }
+      tc::fence_async_smem();
+      tc::named_sync(2, 64);
+      if (ct == 0) {
+        // O += P'(g) V(g); a segment's first PV overwrites O once the
+        // previous segment's epilogue has read it
+        bool w2 = true;
+        if (cfirst && kseg > 0) w2 = mbar_wait(&bar[kOF], (kseg - 1) & 1, a.status, 127);
+        w2 = w2 && mbar_wait(&bar[kPF + (g & 1)], (g >> 1) & 1, a.status, 128);
+        if (w2) {
+          tc::fence_after_sync();
+          const uint32_t pcol = tmem + kColS + (g & 1) * kTile;
+          tc::mma_ts(tmem, pcol, dV, idO, cfirst ? 0u : 1u);
+          tc::mma_ts(tmem, pcol + 8, dV + (2048 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 16, dV + (4096 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 24, dV + (6144 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 32, dV + (8192 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 40, dV + (10240 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 48, dV + (12288 >> 4), idO, 1u);
+          tc::mma_ts(tmem, pcol + 56, dV + (14336 >> 4), idO, 1u);
+          tc::mma_commit(smem_u32(&bar[kPD + (g & 1)]));
+        } else {
+          *conv_fail = 1;
+        }
+      }
+      have = more;
+      cfirst = nfirst;
     }
     if (!ok) *abort_flag = 1;
+    if (ct == 0) tc::mma_commit(smem_u32(&bar[kDR]));   // the value MMAs' completion
   } else {
     // ------------------------------------------------------------ softmax
     // thread = head; x = D * s per key, logits x * sq * scale (log2 domain),

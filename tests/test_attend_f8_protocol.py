@@ -1,19 +1,19 @@
 """Model of the FP8 attention kernel's barrier protocol (CPU only).
 
 attend_f8.cu runs one CTA per (KV split, query token, latent half) with a
-TMA producer, an MMA issuer (the score MMAs of tile g on the four latent
-blocks and the RoPE block, then the value MMA of tile g - 1), two converter
-warps (this half's codes of a tile, loaded from the pool into registers,
-widened to bf16 into one value buffer once the previous value MMA has read
-it) and four softmax warps.  They meet only at mbarriers, and every wait is
-a parity wait.  As for the bf16 kernel's model (test_attend_protocol.py),
-each role's loop is restated -- the order of its waits, arrivals and buffer
-accesses, none of the arithmetic -- and driven in many random interleavings;
-the model fails on deadlock, on a parity wait passing on the wrong phase,
-and when a role reads a buffer that does not hold what it expects (ring
-slot, row scales, S buffer, value buffer, query image, O).  A change to the
-order of waits, arrivals or buffer accesses in the kernel must be made here
-too.
+TMA producer, a score-MMA issuer (the score MMAs of each tile on the four
+latent blocks and the RoPE block), two converter warps (this half's codes of
+a tile, loaded from the pool into registers, widened to bf16 into one value
+buffer once the previous value MMA has read it, then the tile's value MMAs
+issued by one of their threads) and four softmax warps.  They meet only at
+mbarriers, and every wait is a parity wait.  As for the bf16 kernel's model
+(test_attend_protocol.py), each role's loop is restated -- the order of its
+waits, arrivals and buffer accesses, none of the arithmetic -- and driven in
+many random interleavings; the model fails on deadlock, on a parity wait
+passing on the wrong phase, and when a role reads a buffer that does not
+hold what it expects (ring slot, row scales, S buffer, value buffer, query
+image, O).  A change to the order of waits, arrivals or buffer accesses in
+the kernel must be made here too.
 """
 from __future__ import annotations
 
@@ -48,6 +48,7 @@ def run_f8_protocol(segs, half: int, rescale: bool, seed: int | None, drop: str 
     scales = [None, None]         # tile whose scales a buffer holds
     s_buf = [None, None]          # ("S" | "P", tile)
     v_buf = [None]                # tile whose values the buffer holds
+    v_read = [-1]                 # last tile whose value MMAs ran
     q_img = [None]                # segment whose query image is loaded
     o_state = {"seg": None, "last": None}
     live = [(k, s) for k, s in enumerate(segs) if ntiles(s[1], s[2]) > 0]
@@ -74,60 +75,63 @@ def run_f8_protocol(segs, half: int, rescale: bool, seed: int | None, drop: str 
                 g += 1
 
     def mma():
-        g0 = 0
+        g = 0
         for kk, (k, (_, p0, p1)) in enumerate(live):
             n = ntiles(p0, p1)
             yield q_full, kk
-            for i in range(n + 1):
-                gs, gv = g0 + i, g0 + i - 1
-                if i < n:
-                    if gs >= 2:
-                        yield pv_done[gs & 1], (gs - 2) >> 1
-                    expect(s_buf[gs & 1] is None or s_buf[gs & 1] == ("P", gs - 2),
-                           f"S({gs}) over {s_buf[gs & 1]}")
-                    for kb in range(5):
-                        nr = 5 * gs + kb
-                        yield full[nr % RING], nr // RING
-                        expect(ring[nr % RING] == nr, f"S({gs}) block {kb}: slot holds "
-                               f"{ring[nr % RING]}")
-                        expect(q_img[0] == kk, f"S({gs}) with the query of segment {q_img[0]}")
-                        empty[nr % RING].arrive()
-                    s_buf[gs & 1] = ("S", gs)
-                    s_full[gs & 1].arrive()
-                    if i == n - 1:
-                        q_empty.arrive()
-                if i >= 1:
-                    if i == 1 and kk > 0 and "o_free" not in drop:
-                        yield o_free, kk - 1
-                    yield p_full[gv & 1], gv >> 1
-                    if "v_full" not in drop:
-                        yield v_full[gv & 1], gv >> 1
-                    expect(s_buf[gv & 1] == ("P", gv), f"PV({gv}) reads {s_buf[gv & 1]}")
-                    expect(v_buf[0] == gv, f"PV({gv}) reads values of tile {v_buf[0]}")
-                    st = o_state
-                    if i == 1:
-                        expect(st["seg"] is None or st.get("read") == st["seg"],
-                               f"PV({gv}) overwrites O of segment {st['seg']} before its read")
-                        st.clear()
-                        st.update(seg=kk, last=None)
-                    else:
-                        expect(st["last"] == gv - 1, f"PV({gv}) after PV({st['last']})")
-                    expect(st.get("rescaled_for", gv) == gv, "rescale raced a PV")
-                    st["last"] = gv
-                    st.pop("rescaled_for", None)
-                    pv_done[gv & 1].arrive()
-            g0 += n
+            for i in range(n):
+                if g >= 2 and "pv_s" not in drop:
+                    yield pv_done[g & 1], (g - 2) >> 1
+                expect(s_buf[g & 1] is None or s_buf[g & 1] == ("P", g - 2),
+                       f"S({g}) over {s_buf[g & 1]}")
+                for kb in range(5):
+                    nr = 5 * g + kb
+                    yield full[nr % RING], nr // RING
+                    expect(ring[nr % RING] == nr, f"S({g}) block {kb}: slot holds "
+                           f"{ring[nr % RING]}")
+                    expect(q_img[0] == kk, f"S({g}) with the query of segment {q_img[0]}")
+                    empty[nr % RING].arrive()
+                s_buf[g & 1] = ("S", g)
+                s_full[g & 1].arrive()
+                if i == n - 1:
+                    q_empty.arrive()
+                g += 1
 
     def converter():
         g = 0
-        for _, (_, p0, p1) in live:
+        for kk, (_, (_, p0, p1)) in enumerate(live):
             for i in range(ntiles(p0, p1)):
                 # the codes come from the pool (no ring stage), then wait for
                 # the value buffer
                 if g >= 1 and "pv_v" not in drop:
                     yield pv_done[(g - 1) & 1], (g - 1) >> 1
+                expect(v_read[0] >= g - 1, f"values of tile {g} written over those of "
+                       f"tile {v_buf[0]} before PV({g - 1}) ran")
                 v_buf[0] = g
-                v_full[g & 1].arrive()
+                # the value MMAs of tile g, issued by a converter thread
+                if i == 0 and kk > 0 and "o_free" not in drop:
+                    yield o_free, kk - 1
+                yield p_full[g & 1], g >> 1
+
+                # issued here, executed later: the MMAs read P, the value
+                # buffer and O when they run (a pending event)
+                def run_pv(g=g, i=i, kk=kk):
+                    expect(s_buf[g & 1] == ("P", g), f"PV({g}) reads {s_buf[g & 1]}")
+                    expect(v_buf[0] == g, f"PV({g}) reads values of tile {v_buf[0]}")
+                    st = o_state
+                    if i == 0:
+                        expect(st["seg"] is None or st.get("read") == st["seg"],
+                               f"PV({g}) overwrites O of segment {st['seg']} before its read")
+                        st.clear()
+                        st.update(seg=kk, last=None)
+                    else:
+                        expect(st["last"] == g - 1, f"PV({g}) after PV({st['last']})")
+                    expect(st.get("rescaled_for", g) == g, "rescale raced a PV")
+                    st["last"] = g
+                    st.pop("rescaled_for", None)
+                    v_read[0] = g
+                    pv_done[g & 1].arrive()
+                land(run_pv)
                 g += 1
 
     def softmax(w):
@@ -208,13 +212,13 @@ def test_workload_split_plans(name):
             assert run_f8_protocol(segs, c % 2, c % 3 == 0, c) is None, (name, t, c)
 
 
-# The kernel also keeps waits that this ordering already implies, so that
-# leaving one out is no hazard here: the MMA issuer's wait for PV(g - 2)
-# before S(g) (MMAs of one thread complete in issue order) and its wait for
-# the epilogue before a segment's first PV (that PV also waits for P from
-# all four softmax warps, which write the epilogue first).
-SLOW_FOR = {"pv_v": "mma", "v_full": "converter", "c_empty": "softmax", "q_empty": "mma",
-            "pv_rescale": "mma"}
+# The kernel also keeps a wait that the ordering already implies, so that
+# leaving it out is no hazard here: the wait for the epilogue before a
+# segment's first PV (that PV also waits for P from all four softmax warps,
+# which write the epilogue first).  The value MMAs are issued by the thread
+# that wrote the value buffer, so the buffer needs no barrier of its own.
+SLOW_FOR = {"pv_v": "converter", "pv_s": "softmax", "c_empty": "softmax", "q_empty": "mma",
+            "pv_rescale": "converter"}
 
 
 @pytest.mark.parametrize("drop", list(SLOW_FOR))
