@@ -103,45 +103,57 @@ combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__
   *reinterpret_cast<uint2*>(o_lat + (size_t)mh * kLat + q4 * 4) = v;
 }
 
-// The same merge with one thread per (token, head, 4 latent columns), for
-// sequences split into a few pieces only (many (token, head) rows, short
-// loops); the partial rows are read as coalesced float4 runs.
+// The same merge for sequences split into a few pieces only: one CTA per
+// (token, 16 heads), so that a token whose sequence one split held (it wrote
+// o_lat itself) costs one small CTA that leaves at once; a thread takes one
+// head and 8 runs of 4 latent columns, with the 8 loads of a split in flight
+// together (coalesced 256-byte runs per half warp).
+constexpr int kCombineHeads = 16;
 __global__ void __launch_bounds__(256)
 combine_rows_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-               const int* __restrict__ slot_base, int T, int M,
-               __nv_bfloat16* __restrict__ o_lat) {
+                    const int* __restrict__ slot_base, int T, __nv_bfloat16* __restrict__ o_lat) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gid = blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= M * kHeads * (kLat / 4)) return;
-  const int q4 = gid % (kLat / 4), mh = gid / (kLat / 4);
-  const int m = mh / kHeads, head = mh % kHeads;
+  const int m = blockIdx.x / (kHeads / kCombineHeads);
+  const int head = (blockIdx.x % (kHeads / kCombineHeads)) * kCombineHeads + threadIdx.x / 16;
+  const int c4 = threadIdx.x % 16;   // runs c4, c4 + 16, ... of 4 columns
   const int b = m / T, t = m % T;
   const int s0 = slot_base[b], s1 = slot_base[b + 1];
   if (s1 - s0 == 1) return;   // one split held the whole sequence: it wrote o_lat itself
   float lmax = -INFINITY;
   for (int s = s0; s < s1; ++s) lmax = fmaxf(lmax, part_lse[((size_t)s * T + t) * kHeads + head]);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-#pragma unroll 4
   for (int s = s0; s < s1; ++s) {
     const size_t r = ((size_t)s * T + t) * kHeads + head;
     const float w = exp2f(part_lse[r] - lmax);
     wsum += w;
     if (w == 0.f) continue;   // an empty split (no visible token) contributes nothing
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(part_o + r * kLat) + q4);
-    acc.x = fmaf(w, x.x, acc.x);
-    acc.y = fmaf(w, x.y, acc.y);
-    acc.z = fmaf(w, x.z, acc.z);
-    acc.w = fmaf(w, x.w, acc.w);
+    const float4* src = reinterpret_cast<const float4*>(part_o + r * kLat) + c4;
+    float4 x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = __ldcg(src + 16 * j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      acc[j].x = fmaf(w, x[j].x, acc[j].x);
+      acc[j].y = fmaf(w, x[j].y, acc[j].y);
+      acc[j].z = fmaf(w, x[j].z, acc[j].z);
+      acc[j].w = fmaf(w, x[j].w, acc[j].w);
+    }
   }
   const float inv = 1.f / wsum;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 v;
-  v.x = *reinterpret_cast<const uint32_t*>(&lo);
-  v.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(o_lat + (size_t)mh * kLat + q4 * 4) = v;
+  __nv_bfloat16* dst = o_lat + ((size_t)m * kHeads + head) * kLat + c4 * 4;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&lo);
+    v.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst + 64 * j) = v;
+  }
 }
 
 // K splits so that one wave fills the SMs, within the scratch budget.
@@ -422,11 +434,11 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   {
     prof_mark(ctx, st, "combine");
     ctx->launches += 1;
-    // many splits per sequence: a CTA per (token, head); else a thread per
-    // (token, head, 4 columns)
+    // many splits per sequence: a CTA per (token, head); else a CTA per
+    // (token, 16 heads)
     const bool per_head = L.n_slots >= 8 * B;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = per_head ? dim3(M * kHeads) : dim3((M * kHeads * (kLat / 4) + 255) / 256);
+    cfg.gridDim = per_head ? dim3(M * kHeads) : dim3(M * (kHeads / kCombineHeads));
     cfg.blockDim = per_head ? dim3(kCombineThreads) : dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -441,7 +453,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
         per_head ? cudaLaunchKernelEx(&cfg, combine_heads_kernel, part_o, part_lse, slot_base, T,
                                       olat, ctx->status)
                  : cudaLaunchKernelEx(&cfg, combine_rows_kernel, part_o, part_lse, slot_base, T,
-                                      M, olat);
+                                      olat);
     if (!check(e))
       return false;
   }
