@@ -63,6 +63,10 @@ def parse():
     ap.add_argument("--query-path", action="store_true",
                     help="time the step from the hidden states alone (mla_layer_step: the "
                          "query projections W^DQ, W^UQ, W^QR, then append and decode)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling cut: keep the first N sequences of the workload")
+    ap.add_argument("--cache-len", type=int, default=0,
+                    help="profiling cut: every sequence holds this many cached tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -597,6 +601,14 @@ def main():
     rank, local_rank, world = dist_info()
     from synth import workloads as W
     wl = W.config(a.config)
+    if a.batch or a.cache_len:
+        # a smaller case of the same shapes (for profiler captures; not a
+        # benchmark line of the named workload)
+        lens = wl.lens[:a.batch] if a.batch else wl.lens
+        if a.cache_len:
+            lens = [a.cache_len] * len(lens)
+        wl = dataclasses.replace(wl, name=f"{wl.name}-cut-b{len(lens)}" +
+                                 (f"-l{a.cache_len}" if a.cache_len else ""), lens=list(lens))
     if world > 1:
         import torch
         import torch.distributed as dist

@@ -104,8 +104,10 @@ constexpr uint32_t kFVBytes = 2 * 16384;         // V tile: 2 blocks [128 keys][
 constexpr uint32_t kFStage = kFKBytes + kFVBytes;
 constexpr uint32_t kFOffRing = 3 * 16384;        // after the Q tile
 constexpr uint32_t kFOffBar = kFOffRing + 2 * kFStage;
-constexpr uint32_t kFSmem = kFOffBar + 256 + 1024;
+constexpr uint32_t kFOffX = kFOffBar + 256;      // row-max exchange [2 tiles][2 halves][128], l [2][128]
+constexpr uint32_t kFSmem = kFOffX + 4096 + 1024;
 constexpr uint32_t kFColO = 256;                 // TMEM: S0 at 0, S1 at 128, O at 256
+constexpr int kFThreads = 320;                   // producer, MMA issuer, 8 softmax warps
 
 struct FaArgs {
   const int32_t* seq_lens;
@@ -115,7 +117,7 @@ struct FaArgs {
   float scale_log2;
 };
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kFThreads, 1)
 prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 128*192]
                       const __grid_constant__ CUtensorMap tmK,   // K^C [B*Smax, 128*128]
                       const __grid_constant__ CUtensorMap tmR,   // rows [B*Smax, 576]
@@ -128,12 +130,15 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
   uint64_t* full = bar;          // [2] K/V stage loaded
   uint64_t* empty = bar + 2;     // [2] K/V stage consumed
   uint64_t* s_full = bar + 4;    // [2] S of tiles of that parity done
-  uint64_t* p_full = bar + 6;    // [2] P written (4 softmax warps)
+  uint64_t* p_full = bar + 6;    // [2] P written (8 softmax warps)
   uint64_t* pv_done = bar + 8;   // [2] PV of tiles of that parity done
   uint64_t* q_full = bar + 10;
   uint64_t* drained = bar + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* sm_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  float* xmax = reinterpret_cast<float*>(smem + kFOffX);   // [2][2][128]
+  float* xl = xmax + 512;                                    // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, head = blockIdx.y, b = blockIdx.z;
@@ -152,12 +157,13 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], 8);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(drained, 1);
     *abort_flag = 0;
+    *sm_fail = 0;
     tc::fence_barrier_init();
   }
   if (warp == 1) {
@@ -259,8 +265,16 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
     if (el) tc::mma_commit(smem_u32(drained));
   } else {
     // ---------------------------------------------------------- softmax
-    // Thread = query row.  Keys up to the query's own position are visible.
+    // Eight warps: warps w and w + 4 share TMEM lanes 32 (w % 4).. (thread =
+    // query row) and take keys 0..63 and 64..127 of each tile (and O columns
+    // 0..63 and 64..127).  The two halves of a row exchange their maxima
+    // through shared memory at a barrier of the 256 softmax threads, so
+    // both take the same maximum and rescale decision; l is kept per half
+    // and summed at the end.  Keys up to the query's own position are
+    // visible.  A failed wait raises sm_fail, which every thread reads after
+    // the next barrier, so all 256 leave together.
     const int q4 = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q4 * 32 + lane;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const int qpos = q0 + row;
@@ -269,67 +283,87 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int s = j & 1;
-      if (!bar_wait<false>(&s_full[s], (j >> 1) & 1, a.status, 106)) ok = false;
-      if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
+      if (!bar_wait<false>(&s_full[s], (j >> 1) & 1, a.status, 106) || *abort_flag) *sm_fail = 1;
       tc::fence_after_sync();
-      uint32_t lo[64], hi[64];
-      tc::tmem_ld64(trow + s * kFK, lo);
-      tc::tmem_ld64(trow + s * kFK + 64, hi);
+      uint32_t v[64];
+      tc::tmem_ld64(trow + s * kFK + half * 64, v);
       const int valid = live ? max(0, min(kFK, qpos - j * kFK + 1)) : 0;
-      const float mx = (valid == kFK ? row_max<false>(lo, hi, valid)
-                                     : row_max<true>(lo, hi, valid)) * a.scale_log2;
+      const int vh = max(0, min(64, valid - half * 64));   // visible keys of this half
+      float mh = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (c < vh) mh = fmaxf(mh, __uint_as_float(v[c]));
+      xmax[(s * 2 + half) * 128 + row] = mh;
+      tc::named_sync(1, 256);
+      if (*sm_fail) { ok = false; break; }   // read after the barrier: the same for all
+      const float mx = fmaxf(mh, xmax[(s * 2 + (half ^ 1)) * 128 + row]) * a.scale_log2;
       const bool need = j > 0 && mx > m_used + kRescale;
       if (j == 0) {
         m_used = mx;
       } else if (__any_sync(0xffffffffu, need)) {
-        // O holds PV(0..j-1): rescale once PV(j - 1) is done
-        if (!bar_wait<false>(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status, 107)) ok = false;
-        if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+        // O holds PV(0..j-1): rescale this half's columns once PV(j - 1) is done
+        if (!bar_wait<false>(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.status, 107))
+          *sm_fail = 1;
         tc::fence_after_sync();
         const float m_new = need ? mx : m_used;
         const float f = exp2f(m_used - m_new);
         l *= f;
-        for (int c0 = 0; c0 < kDv; c0 += 16) {
-          float v[16];
-          tc::tmem_ld16(trow + kFColO + c0, v);
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          float o[16];
+          tc::tmem_ld16(trow + kFColO + half * 64 + c0, o);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) v[jj] *= f;
-          tc::tmem_st16(trow + kFColO + c0, v);
+          for (int jj = 0; jj < 16; ++jj) o[jj] *= f;
+          tc::tmem_st16(trow + kFColO + half * 64 + c0, o);
         }
         m_used = m_new;
       }
-      uint32_t pk[64];
-      const float psum = valid == kFK ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
-                                      : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
+      // P (bf16, two keys per column) over this half's S columns: keys
+      // half*64 + 2i, +1 -> column half*32 + i (the S MMA of j + 2 waits for
+      // PV(j) before reusing the buffer)
+      uint32_t pk[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c0 = 2 * i, c1 = 2 * i + 1;
+        const float e0 = c0 < vh ? tc::ex2_approx(fmaf(__uint_as_float(v[c0]), a.scale_log2, -m_used)) : 0.f;
+        const float e1 = c1 < vh ? tc::ex2_approx(fmaf(__uint_as_float(v[c1]), a.scale_log2, -m_used)) : 0.f;
+        psum += e0 + e1;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+        pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
       l += psum;
-      // P(j) over S(j) (the S MMA of j + 2 waits for PV(j) before reusing it)
-      tc::tmem_st64(trow + s * kFK, pk);
+      tc::tmem_st32(trow + s * kFK + half * 32, pk);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(smem_u32(&p_full[s]));
     }
-    if (ok) {
-      ok = bar_wait<false>(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, 108);
-      if (__any_sync(0xffffffffu, !ok)) ok = false;
-    }
-    if (ok) {
+    // epilogue: l of both halves, then O / l of this half's 64 columns
+    if (ok && !bar_wait<false>(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, 108))
+      *sm_fail = 1;
+    xl[half * 128 + row] = l;
+    tc::named_sync(1, 256);
+    if (ok && !*sm_fail) {
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = a.o + ((size_t)(b * a.T + t0 + row)) * (kHeads * kDv) + head * kDv;
-      for (int c0 = 0; c0 < kDv; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(trow + kFColO + c0, v);
+      const float lt = l + xl[(half ^ 1) * 128 + row];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* dst =
+          a.o + ((size_t)(b * a.T + t0 + row)) * (kHeads * kDv) + head * kDv + half * 64;
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float o[16];
+        tc::tmem_ld16(trow + kFColO + half * 64 + c0, o);
         if (live) {
           uint32_t w[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * jj] * inv, v[2 * jj + 1] * inv);
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * jj] * inv, o[2 * jj + 1] * inv);
             w[jj] = *reinterpret_cast<const uint32_t*>(&h2);
           }
           *reinterpret_cast<uint4*>(dst + c0) = make_uint4(w[0], w[1], w[2], w[3]);
           *reinterpret_cast<uint4*>(dst + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
+    } else {
+      ok = false;
     }
     if (!ok) *abort_flag = 1;
   }
@@ -444,7 +478,7 @@ bool bf16_prefill_explicit(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bflo
     static std::atomic<uint64_t> attr_done{0};
     if (smem_attr_once(attr_done, prefill_attend_kernel, (int)kFSmem) != cudaSuccess) return false;
     cudaLaunchConfig_t cfg =
-        pdl_cfg(dim3((T + kFQ - 1) / kFQ, kHeads, B), dim3(192), kFSmem, st, attr);
+        pdl_cfg(dim3((T + kFQ - 1) / kFQ, kHeads, B), dim3(kFThreads), kFSmem, st, attr);
     prof_mark(ctx, st, "prefill_attend");
     ctx->launches += 1;
     if (cudaLaunchKernelEx(&cfg, prefill_attend_kernel, tmQ, tmK, tmR, tmV, fa) != cudaSuccess)
