@@ -95,26 +95,28 @@ def load_peaks():
             "source": "fallback"}
 
 
-def csrc_hash() -> str:
-    import glob
+def sources_hash(files) -> str:
+    """sha256 (16 hex digits) of the named files under the package's csrc/."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "mla_latent_kv_82_b300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in sorted(files):
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "mla_latent_kv_82_b300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def captured_traffic(config_key: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    """DRAM bytes per launch of `kernel` on workload `config_key` from the
+    committed ncu summary, if the kernel's sources still hash as they did
+    when it was captured."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f).get(config_key, {}).get(kernel)
-    except (OSError, ValueError):
-        return None
-    if not rec or rec.get("csrc_sha256_16") != csrc_hash():
+        if not rec or rec.get("sources_sha256_16") != sources_hash(rec["sources"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     return rec["dram_bytes"]
 
@@ -492,7 +494,9 @@ def run_mla(a, wl, rank, local_rank, world):
         roof = {"bound": "tensor", "achieved": f_dom / t_dom / 1e12, "peak": tf_peak,
                 "unit": "TFLOP/s"}
     roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": dom,
-                 "traffic": captured_traffic(a.config, dom), "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
+                 "traffic": None if (a.batch or a.cache_len) else
+                 captured_traffic(a.config + ("+fp8" if a.kv == "fp8" else ""), dom),
+                 "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json)"
                  if peaks["source"] == "measured" else "fallback",
                  "algorithmic_bytes_per_launch": b_dom, "algorithmic_flops_per_launch": f_dom,
                  "avg_launch_ms": avg[dom],

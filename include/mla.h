@@ -246,7 +246,7 @@ size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T,
  * token (absorbed query, combine, W^UV).  With S = max_pages·page_size keys
  * per sequence: the explicit form for prompts on an empty cache from a few
  * dozen tokens up, the absorbed form for decode and for short chunks after
- * a long prefix (below about 460 tokens after 12288).  fp32 contexts, FP8
+ * a long prefix (below about 380 tokens after 12288).  fp32 contexts, FP8
  * caches, and calls whose batch·max_pages·page_size exceeds
  * 2^18 rows, always get MLA_FORM_ABSORBED. */
 int mla_prefill_form(const mla_ctx* ctx, int batch, int T, int max_pages);

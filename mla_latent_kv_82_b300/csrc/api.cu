@@ -353,13 +353,13 @@ size_t mla_prefill_workspace_size(const mla_ctx* ctx, int batch, int T, int max_
 // each against up to S keys, from per-unit costs of this library's kernels
 // measured on B300 at DeepSeek-V2 widths (ns).  Explicit: 65 per cached key
 // (gather, K^C and V up-projections), 16 per query token (rotated queries),
-// 0.11 per visible (query, key) pair (2·128·320 FLOP).  Absorbed: 190 per
+// 0.08 per visible (query, key) pair (2·128·320 FLOP).  Absorbed: 190 per
 // query token (absorbed query, combine, W^UV) and 0.24 per pair
 // (2·128·1088 FLOP).  The append and W_O are common to both.
 static bool explicit_is_cheaper(int batch, int T, long long S) {
   const double B = batch, t = T, s = (double)S;
   const double pairs = B * t * (s - 0.5 * (t - 1.0));
-  const double expl = 65.0 * B * s + 16.0 * B * t + 0.11 * pairs;
+  const double expl = 65.0 * B * s + 16.0 * B * t + 0.08 * pairs;
   const double absd = 190.0 * B * t + 0.24 * pairs;
   return expl < absd;
 }

@@ -101,9 +101,9 @@ constexpr int kFQ = 128;                         // query rows per CTA
 constexpr int kFK = 128;                         // keys per tile
 constexpr uint32_t kFKBytes = 3 * 16384;         // K tile: 3 blocks [128 keys][64 features]
 constexpr uint32_t kFVBytes = 2 * 16384;         // V tile: 2 blocks [128 keys][64 columns]
-constexpr uint32_t kFStage = kFKBytes + kFVBytes;
-constexpr uint32_t kFOffRing = 3 * 16384;        // after the Q tile
-constexpr uint32_t kFOffBar = kFOffRing + 2 * kFStage;
+constexpr uint32_t kFOffK = 3 * 16384;           // two K stages after the Q tile
+constexpr uint32_t kFOffV = kFOffK + 2 * kFKBytes;   // two V stages
+constexpr uint32_t kFOffBar = kFOffV + 2 * kFVBytes;
 constexpr uint32_t kFOffX = kFOffBar + 256;      // row-max exchange [2 tiles][2 halves][128], l [2][128]
 constexpr uint32_t kFSmem = kFOffX + 4096 + 1024;
 constexpr uint32_t kFColO = 256;                 // TMEM: S0 at 0, S1 at 128, O at 256
@@ -127,14 +127,19 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFOffBar);
-  uint64_t* full = bar;          // [2] K/V stage loaded
-  uint64_t* empty = bar + 2;     // [2] K/V stage consumed
+  // K and V stream through separate two-stage rings: K(j) is released when
+  // S(j) completes and V(j) when PV(j) does, so K(j + 2) loads while the
+  // softmax of tile j runs
+  uint64_t* kfull = bar;         // [2] K stage loaded
+  uint64_t* kempty = bar + 2;    // [2] K stage consumed (S done)
   uint64_t* s_full = bar + 4;    // [2] S of tiles of that parity done
   uint64_t* p_full = bar + 6;    // [2] P written (8 softmax warps)
   uint64_t* pv_done = bar + 8;   // [2] PV of tiles of that parity done
   uint64_t* q_full = bar + 10;
   uint64_t* drained = bar + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* vfull = bar + 12;    // [2] V stage loaded
+  uint64_t* vempty = bar + 14;   // [2] V stage consumed (PV done)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* sm_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
   float* xmax = reinterpret_cast<float*>(smem + kFOffX);   // [2][2][128]
@@ -154,8 +159,10 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
       mbar_init(&pv_done[i], 1);
@@ -174,7 +181,7 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  int issued = 0;
+  int k_issued = 0, v_issued = 0;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -189,24 +196,42 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
         tc::tma_load_2d(smem_u32(smem + blk * 16384), &tmQ, head * (kNope + kRope) + blk * 64,
                         b * a.T + t0, smem_u32(q_full));
     }
-    for (int j = 0; j < n; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !warp_wait<false>(&empty[s], ((j >> 1) - 1) & 1, a.status, 101)) {
-        *abort_flag = 1;
-        break;
+    // K one tile ahead of V: K(0), K(1), V(0), K(2), V(1), ...
+    for (int j = 0; j <= n; ++j) {
+      if (j < n) {
+        const int s = j & 1;
+        if (j >= 2 && !warp_wait<false>(&kempty[s], ((j >> 1) - 1) & 1, a.status, 101)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        k_issued = j + 1;
+        if (el) {
+          const uint32_t st = smem_u32(smem + kFOffK + s * kFKBytes);
+          const uint32_t fb = smem_u32(&kfull[s]);
+          const int y = krow0 + j * kFK;
+          tc::mbar_arrive_expect_tx(fb, kFKBytes);
+          tc::tma_load_2d(st, &tmK, head * kNope, y, fb);
+          tc::tma_load_2d(st + 16384, &tmK, head * kNope + 64, y, fb);
+          tc::tma_load_2d(st + 32768, &tmR, kLat, y, fb);
+        }
       }
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      issued = j + 1;
-      if (el) {
-        const uint32_t st = smem_u32(smem + kFOffRing + s * kFStage);
-        const uint32_t fb = smem_u32(&full[s]);
-        const int y = krow0 + j * kFK;
-        tc::mbar_arrive_expect_tx(fb, kFStage);
-        tc::tma_load_2d(st, &tmK, head * kNope, y, fb);
-        tc::tma_load_2d(st + 16384, &tmK, head * kNope + 64, y, fb);
-        tc::tma_load_2d(st + 32768, &tmR, kLat, y, fb);
-        tc::tma_load_2d(st + kFKBytes, &tmV, head * kDv, y, fb);
-        tc::tma_load_2d(st + kFKBytes + 16384, &tmV, head * kDv + 64, y, fb);
+      if (j >= 1) {
+        const int jv = j - 1, s = jv & 1;
+        if (jv >= 2 && !warp_wait<false>(&vempty[s], ((jv >> 1) - 1) & 1, a.status, 109)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        v_issued = jv + 1;
+        if (el) {
+          const uint32_t st = smem_u32(smem + kFOffV + s * kFVBytes);
+          const uint32_t fb = smem_u32(&vfull[s]);
+          const int y = krow0 + jv * kFK;
+          tc::mbar_arrive_expect_tx(fb, kFVBytes);
+          tc::tma_load_2d(st, &tmV, head * kDv, y, fb);
+          tc::tma_load_2d(st + 16384, &tmV, head * kDv + 64, y, fb);
+        }
       }
     }
   } else if (warp == 1) {
@@ -217,8 +242,8 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
     constexpr uint32_t idS = tc::idesc_bf16(128, kFK, false, false);
     constexpr uint32_t idO = tc::idesc_bf16(128, kDv, false, true);
     const uint64_t dQ = tc::sdesc(smem_u32(smem), 16, 1024);
-    const uint64_t dR = tc::sdesc(smem_u32(smem + kFOffRing), 16, 1024);
-    const uint64_t dV = tc::sdesc(smem_u32(smem + kFOffRing + kFKBytes), 16384, 1024);
+    const uint64_t dR = tc::sdesc(smem_u32(smem + kFOffK), 16, 1024);
+    const uint64_t dV = tc::sdesc(smem_u32(smem + kFOffV), 16384, 1024);
     bool ok = warp_wait<false>(q_full, 0, a.status, 102);
     for (int j = 0; ok && j <= n; ++j) {
       if (j < n) {
@@ -227,11 +252,11 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
           ok = false;
           break;
         }
-        if (!warp_wait<false>(&full[s], (j >> 1) & 1, a.status, 104)) { ok = false; break; }
+        if (!warp_wait<false>(&kfull[s], (j >> 1) & 1, a.status, 104)) { ok = false; break; }
         tc::fence_after_sync();
         if (el) {
           const uint32_t d = tmem + s * kFK;
-          const uint64_t dk = dR + ((s * kFStage) >> 4);
+          const uint64_t dk = dR + ((s * kFKBytes) >> 4);
           // straight-line MMAs (a branch between MMAs slows their issue)
 #pragma unroll
           for (int blk = 0; blk < 3; ++blk) {
@@ -241,23 +266,28 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
             tc::mma_ss(d, qa + 4, kb + 4, idS, 1u);
             tc::mma_ss(d, qa + 6, kb + 6, idS, 1u);
           }
+          tc::mma_commit(smem_u32(&kempty[s]));
           tc::mma_commit(smem_u32(&s_full[s]));
         }
       }
       if (j >= 1) {
         const int jv = j - 1, s = jv & 1;
-        if (!warp_wait<false>(&p_full[s], (jv >> 1) & 1, a.status, 105)) { ok = false; break; }
+        if (!warp_wait<false>(&p_full[s], (jv >> 1) & 1, a.status, 105) ||
+            !warp_wait<false>(&vfull[s], (jv >> 1) & 1, a.status, 110)) {
+          ok = false;
+          break;
+        }
         if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         tc::fence_after_sync();
         if (el) {
           const uint32_t pcol = tmem + s * kFK;
-          const uint64_t vb = dV + ((s * kFStage) >> 4);
+          const uint64_t vb = dV + ((s * kFVBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)   // 16 keys per K step: 8 P columns, 2 atoms of V
             tc::mma_ts(tmem + kFColO, pcol + 8 * kk, vb + kk * (2048 >> 4), idO,
                        (jv > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(smem_u32(&pv_done[s]));
-          tc::mma_commit(smem_u32(&empty[s]));
+          tc::mma_commit(smem_u32(&vempty[s]));
         }
       }
     }
@@ -373,16 +403,20 @@ prefill_attend_kernel(const __grid_constant__ CUtensorMap tmQ,   // q_rot [B*T, 
   __syncthreads();
   if (threadIdx.x == 0) {
     if (*abort_flag) {
-      mbar_wait(q_full, 0, a.status, 109, 1 << 20, 100000000ull);
-      for (int i = 0; i < 2 && i < issued; ++i) {
-        const int u = issued - 1 - i;
-        mbar_wait(&full[u & 1], (u >> 1) & 1, a.status, 110, 1 << 20, 100000000ull);
+      mbar_wait(q_full, 0, a.status, 111, 1 << 20, 100000000ull);
+      for (int i = 0; i < 2 && i < k_issued; ++i) {
+        const int u = k_issued - 1 - i;
+        mbar_wait(&kfull[u & 1], (u >> 1) & 1, a.status, 112, 1 << 20, 100000000ull);
+      }
+      for (int i = 0; i < 2 && i < v_issued; ++i) {
+        const int u = v_issued - 1 - i;
+        mbar_wait(&vfull[u & 1], (u >> 1) & 1, a.status, 113, 1 << 20, 100000000ull);
       }
     }
   }
   __syncthreads();
   if (warp == 1) {
-    mbar_wait(drained, 0, a.status, 111, 1 << 20, 100000000ull);
+    mbar_wait(drained, 0, a.status, 114, 1 << 20, 100000000ull);
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
