@@ -142,9 +142,10 @@ class StackState:
     ``step()`` runs mla_multi_layer_step on the new tokens' layer-0 hidden
     states (copied into ``h`` first, so every step repeats the same work)."""
 
-    def __init__(self, wl, device: int = 0, chunk: int = 32768):
+    def __init__(self, wl, device: int = 0, chunk: int = 32768, kv: str = "native"):
         from . import MLA
         self.wl = wl
+        self.kv = kv
         self.dev = torch.device("cuda", device)
         d, dt, T = wl.dims, wl.torch_dtype, wl.T
         bt = wl.block_table()
@@ -155,8 +156,11 @@ class StackState:
         for j in range(wl.layers):
             w = {n: wl.weight(n, device=self.dev, layer=j) for n in W_NAMES + Q_NAMES}
             self.weights.append(w)
-            self.mlas.append(MLA(d, w, wl.dtype, max_position=max(wl.seq_lens), device=device))
-            self.caches.append(torch.empty((rows, d.row_width), dtype=dt, device=self.dev))
+            self.mlas.append(MLA(d, w, wl.dtype, max_position=max(wl.seq_lens), device=device,
+                                 kv=kv))
+            self.caches.append(torch.empty((rows, 656), dtype=torch.uint8, device=self.dev)
+                               if kv == "fp8" else
+                               torch.empty((rows, d.row_width), dtype=dt, device=self.dev))
         self.seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=self.dev)
         self.pos_new = torch.tensor([L + t for L in wl.lens for t in range(T)],
                                     dtype=torch.int32, device=self.dev)

@@ -15,6 +15,8 @@ the unchanged explicit decode over the dequantised rows.  Checked:
   max|err| <= 0.1 max|ref| and sum|err| / sum|ref| <= 0.03;
 * the format's own cost: u over the FP8 cache against the exact decode.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -183,3 +185,64 @@ def test_fp8_needs_a_bf16_context():
     with pytest.raises(m.MLAError) as e:
         m.MLA(dataclasses.replace(d, d_cq=0), w, "f32", max_position=8, kv="fp8")
     assert e.value.code == m.MLA_ERR_UNSUPPORTED
+
+
+QNAMES = ("w_dkv", "w_kr", "w_uk", "w_uv", "w_o", "w_dq", "w_uq", "w_qr")
+
+
+def test_layer_step_on_fp8_cache():
+    """mla_layer_step (queries from the hidden states) over an FP8 pool: the
+    oracle makes the queries with query_from_hidden and decodes over its own
+    quantised rows."""
+    from mla_latent_kv_82_b300.workload import DeviceState
+    wl = W.Workload("v2-small-qp-fp8", dataclasses.replace(W.V2, d_model=512), "bf16",
+                    [0, 70, 300], 2, True)
+    st = DeviceState(wl, query_path=True, kv="fp8")
+    st.layer_step()
+    torch.cuda.synchronize()
+    assert st.mla.check_status() == 0
+    w64 = ocase.weights_f64(wl, names=QNAMES, device=DEV)
+    for b in range(wl.B):
+        rows = ocase.sequence_rows(wl, b, w64, device=DEV)
+        q = fp8.quantize_rows(rows, wl.dims.d_latent)
+        check_rows(_pool_bytes(st, b), q)
+        L = wl.lens[b]
+        h = wl.h_rows(b, L, L + wl.T, device=DEV).to(torch.float64).cpu().numpy()
+        qq = omla.query_from_hidden(wl.dims, h, w64["w_dq"], w64["w_uq"], w64["w_qr"])
+        ref = omla.decode_explicit(wl.dims, q["deq"], qq, w64, wl.T)
+        s = omla.error_stats(to_np(st.out[b]), ref["u"])
+        assert s["max_rel"] <= TOL_FP8[0] and s["mean_rel"] <= TOL_FP8[1], f"u b={b}: {s}"
+
+
+def test_layer_stack_on_fp8_cache():
+    """mla_multi_layer_step through three layers with FP8 pools: the oracle
+    runs the stack (h_{j+1} = h_j + u_j) with every layer's rows, cached and
+    new, quantised as the pools hold them.  Each layer's rounding reaches the
+    next layer's input, so to first order the per-layer bounds add: the final
+    h is held to the FP8 bounds times the number of layers."""
+    from mla_latent_kv_82_b300.workload import StackState
+    wl = W.Workload("v2-small-stack-fp8", dataclasses.replace(W.V2, d_model=512), "bf16",
+                    [5, 130], 1, True, layers=3)
+    st = StackState(wl, kv="fp8")
+    st.step()
+    torch.cuda.synchronize()
+    assert st.check_status() == 0
+    d = wl.dims
+    for b in range(wl.B):
+        L, S = wl.lens[b], wl.seq_lens[b]
+        h = wl.h_rows(b, L, L + wl.T, device=DEV).to(torch.float64).cpu().numpy()
+        for j in range(wl.layers):
+            w = {n: wl.weight(n, device=DEV, layer=j).to(torch.float64).cpu().numpy()
+                 for n in QNAMES}
+            hp = wl.h_rows(b, 0, L, device=DEV, layer=j).to(torch.float64).cpu().numpy()
+            rows = np.concatenate([
+                omla.latent_rows(hp, w["w_dkv"], w["w_kr"], np.arange(L), d.rope_base),
+                omla.latent_rows(h, w["w_dkv"], w["w_kr"], np.arange(L, S), d.rope_base)])
+            deq = fp8.quantize_rows(rows, d.d_latent)["deq"]
+            q = omla.query_from_hidden(d, h, w["w_dq"], w["w_uq"], w["w_qr"])
+            u = omla.decode_explicit(d, deq, q, w, wl.T)["u"]
+            h = h + u
+        m = slice(b * wl.T, (b + 1) * wl.T)
+        s = omla.error_stats(to_np(st.h[m]), h)
+        k = wl.layers
+        assert s["max_rel"] <= TOL_FP8[0] * k and s["mean_rel"] <= TOL_FP8[1] * k, f"h b={b}: {s}"
