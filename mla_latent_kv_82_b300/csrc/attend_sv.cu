@@ -100,6 +100,14 @@ enum : int {
   kBSlot = 50      // TMEM base address (u32) and abort flag (u32)
 };
 
+// One 32-byte store (a whole L2 sector per thread: the epilogue writes a
+// row per thread, so 16-byte stores would fill half of each sector).
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.cg.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 constexpr uint32_t kColQ = 0;     // score: q~ (256 columns)
 constexpr uint32_t kColS = 256;   // score: S buffers at 256 and 384
 
@@ -418,7 +426,6 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       }
       // ---- q~ of this segment's token: image blocks 0-7, row `row`
       if (!fail && k > 0) fail = !cwait<kPair>(&bar[kBQEmpty], (k - 1) & 1, a.status, 76);
-      if (!fail) fail = !warp_wait<false>(&bar[kBQr], k & 1, a.status, 77);
       if (!fail) {
         tc::fence_after_sync();
         const uint8_t* img = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes + prow_off;
@@ -445,8 +452,10 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
           }
         }
         tc::fence_before_sync();
+        // the RoPE block lands in parallel; q~ and it are ready together
+        fail = !warp_wait<false>(&bar[kBQr], k & 1, a.status, 77);
         __syncwarp();
-        if (lane == 0) {
+        if (!fail && lane == 0) {
           if (kPair) tc::mbar_arrive_cluster_relaxed(cbar(kBQReady, lead_rank));
           else tc::mbar_arrive(smem_u32(&bar[kBQReady]));
         }
@@ -738,26 +747,32 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
         // the sequence lies in this split alone: O / l is its latent output
         // (bf16, as the combine would write it); the combine skips it
         __nv_bfloat16* od = a.o_lat + (((size_t)sb * a.T + t) * kHeads + row) * kLat;
-        for (int c0 = 0; c0 < kLat; c0 += 16) {
-          float v[16];
-          tc::tmem_ld16(trow + c0, v);
-          uint32_t w[8];
+        for (int c0 = 0; c0 < kLat; c0 += 64) {
+          uint32_t v[64];
+          tc::tmem_ld64(trow + c0, v);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * j] * inv, v[2 * j + 1] * inv);
-            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          for (int j = 0; j < 64; j += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[j + 2 * e]) * inv,
+                                                              __uint_as_float(v[j + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            st_v8(od + c0 + j, w);
           }
-          *reinterpret_cast<uint4*>(od + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(od + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       } else {
-        for (int c0 = 0; c0 < kLat; c0 += 16) {
-          float v[16];
-          tc::tmem_ld16(trow + c0, v);
+        for (int c0 = 0; c0 < kLat; c0 += 64) {
+          uint32_t v[64];
+          tc::tmem_ld64(trow + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            __stcg(reinterpret_cast<float4*>(dst + c0 + j),
-                   make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
+          for (int j = 0; j < 64; j += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[j + e]) * inv);
+            st_v8(dst + c0 + j, w);
+          }
         }
       }
       tc::fence_before_sync();

@@ -325,6 +325,47 @@ static bool append_plan(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T, cons
   return true;
 }
 
+// Arguments of the CUDA-core projection kernel for M <= 2 tokens: the append
+// of h (if given) and the absorbed query of q (if given).
+static SmallProjArgs small_proj_args(const mla_ctx* ctx, int M, int T, const __nv_bfloat16* h,
+                                     const WgArgs* app, const __nv_bfloat16* q, void* qimg) {
+  SmallProjArgs sp{};
+  sp.M = M;
+  sp.T = T;
+  sp.D = ctx->cfg.d_model;
+  sp.h = h;
+  sp.w_dkv = static_cast<const __nv_bfloat16*>(ctx->w.w_dkv);
+  sp.w_kr = static_cast<const __nv_bfloat16*>(ctx->w.w_kr);
+  if (h && app) {
+    sp.pos = app->pos;
+    sp.bt = app->bt;
+    sp.max_pages = app->max_pages;
+    sp.num_pages = app->num_pages;
+    sp.stage_rows = app->stage_rows;
+    sp.cache = app->cache;
+  }
+  sp.q = q;
+  sp.w_uk = static_cast<const __nv_bfloat16*>(ctx->w.w_uk);
+  sp.qimg = static_cast<__nv_bfloat16*>(qimg);
+  sp.rope_cs = ctx->rope_cs;
+  sp.max_position = ctx->cfg.max_position;
+  sp.status = ctx->status;
+  return sp;
+}
+
+// The append of a plan's M rows: the CUDA-core projection kernel for one or
+// two tokens, else the weight-streaming GEMM.
+static bool launch_append(mla_ctx* ctx, const __nv_bfloat16* h, int M, const WgPlan& p,
+                          cudaStream_t st) {
+  prof_mark(ctx, st, "compress_append");
+  ctx->launches += 1;
+  if (M <= kGemvMaxTokens) {
+    SmallProjArgs sp = small_proj_args(ctx, M, p.args.T, h, &p.args, nullptr, nullptr);
+    if (proj_small_supported(sp, ctx->num_sms)) return check(proj_small_launch(sp, ctx->num_sms, st));
+  }
+  return check(wgemm_launch(p, WG_APPEND, false, st, true));
+}
+
 bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                           const int32_t* pos, const int32_t* bt, int max_pages,
                           __nv_bfloat16* cache, int num_pages, cudaStream_t st) {
@@ -339,9 +380,7 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
                        num_pages, p))
         return false;
       p.args.stage_rows = 1;
-      prof_mark(ctx, st, "compress_append");
-      ctx->launches += 1;
-      if (!check(wgemm_launch(p, WG_APPEND, false, st, true))) return false;
+      if (!launch_append(ctx, h + (size_t)m0 * D, mc, p, st)) return false;
       if (!f8_prepare(ctx, ctx->stage, mc, m0, pos, bt, T, max_pages,
                       reinterpret_cast<uint8_t*>(cache), num_pages, nullptr, 0, nullptr, st)) {
         cudaGetLastError();
@@ -352,15 +391,26 @@ bool bf16_compress_append(mla_ctx* ctx, const __nv_bfloat16* h, int B, int T,
   }
   WgPlan p;
   if (!append_plan(ctx, h, B, T, pos, bt, max_pages, cache, num_pages, p)) return false;
-  prof_mark(ctx, st, "compress_append");
-  ctx->launches += 1;
-  return check(wgemm_launch(p, WG_APPEND, false, st, true));
+  return launch_append(ctx, h, B * T, p, st);
 }
+
+static bool decode_impl(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+                        int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
+                        int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
+                        cudaStream_t st, const WgPlan* append, const __nv_bfloat16* append_h);
 
 bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
                  int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
                  int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
                  cudaStream_t st, const WgPlan* append) {
+  return decode_impl(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st,
+                     append, nullptr);
+}
+
+static bool decode_impl(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cache,
+                        int num_pages, const int32_t* bt, int max_pages, const int32_t* seq_lens,
+                        int B, int T, __nv_bfloat16* out, char* ws, const WsLayout& L,
+                        cudaStream_t st, const WgPlan* append, const __nv_bfloat16* append_h) {
   const int M = B * T, D = ctx->cfg.d_model;
   const Bf16Plans bp = decode_plans(ctx, M);
   if (bp.abs.n_tiles > 65535 || bp.uv.n_tiles > 65535 || bp.o.n_tiles > 65535) return false;
@@ -370,7 +420,22 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   float* part = reinterpret_cast<float*>(ws + L.wg_part);
 
   // ---- absorbed query: W^UK_i^T q^C_i (+ rotated q^R) -> query image
-  {
+  SmallProjArgs sp = small_proj_args(ctx, M, T, append ? append_h : nullptr,
+                                     append ? &append->args : nullptr, q, qimg);
+  sp.plan = PlanArgs{seq_lens, B, T, kPage, max_pages, ctx->cfg.max_position, L.G,
+                     reinterpret_cast<int*>(ws + L.lens), reinterpret_cast<int*>(ws + L.page_prefix),
+                     reinterpret_cast<int*>(ws + L.first_split),
+                     reinterpret_cast<int*>(ws + L.slot_base), reinterpret_cast<int*>(ws + L.meta),
+                     ctx->status};
+  sp.do_plan = 1;
+  if (append && append_h == nullptr) return false;   // an append plan comes with its h
+  const bool small = M <= kGemvMaxTokens && proj_small_supported(sp, ctx->num_sms);
+  if (small) {
+    // one or two tokens: matrix-vector products on CUDA cores
+    prof_mark(ctx, st, append ? "append_absorb" : "absorb_q");
+    ctx->launches += 1;
+    if (!check(proj_small_launch(sp, ctx->num_sms, st))) return false;
+  } else {
     WgPlan p{};
     p.nt = bp.abs.nt;
     p.n_tiles = bp.abs.n_tiles;
@@ -399,17 +464,14 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
                       reinterpret_cast<int*>(ws + L.first_split),
                       reinterpret_cast<int*>(ws + L.slot_base), reinterpret_cast<int*>(ws + L.meta),
                       ctx->status};
-    if (append && (append->nt == 16 || append->nt == 32)) {
+    if (append && (append->nt == 16 || append->nt == 32) && M > kGemvMaxTokens) {
       // the append and the absorbed query share no data: one launch
       prof_mark(ctx, st, "append_absorb");
       ctx->launches += 1;
       if (!check(wgemm_launch_dual(*append, p, st, true))) return false;
     } else {
-      if (append) {
-        prof_mark(ctx, st, "compress_append");
-        ctx->launches += 1;
-        if (!check(wgemm_launch(*append, WG_APPEND, false, st, true))) return false;
-      }
+      // (one or two tokens: the append as mla_compress_append runs it)
+      if (append && !launch_append(ctx, append_h, M, *append, st)) return false;
       prof_mark(ctx, st, "absorb_q");
       ctx->launches += 1;
       if (!check(wgemm_launch(p, WG_QIMG, true, st, true))) return false;
@@ -430,8 +492,21 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
   } else if (!sv_attend(ctx, qimg, cache, num_pages, bt, max_pages, B, T, ws, L, st)) {
     return false;
   }
+  // ---- one or two query tokens: the combine and W^UV in one weight-streaming
+  // kernel (o_lat is merged in the CTAs that read W^UV)
+  const float* part_o = reinterpret_cast<const float*>(ws + L.part_o);
+  const float* part_lse = reinterpret_cast<const float*>(ws + L.part_lse);
+  const int* slot_base = reinterpret_cast<const int*>(ws + L.slot_base);
+  CombineValueArgs cv{static_cast<const __nv_bfloat16*>(ctx->w.w_uv), kHeads, M, T, L.n_slots,
+                      part_o, part_lse, slot_base, olat, o, ctx->status};
+  const bool fused_uv = combine_value_supported(cv, ctx->num_sms);
+  if (fused_uv) {
+    prof_mark(ctx, st, "combine_uv");
+    ctx->launches += 1;
+    if (!check(combine_value_launch(cv, ctx->num_sms, st))) return false;
+  }
   // ---- log-sum-exp combine -> o_lat (bf16)
-  {
+  if (!fused_uv) {
     prof_mark(ctx, st, "combine");
     ctx->launches += 1;
     // many splits per sequence: a CTA per (token, head); else a CTA per
@@ -446,9 +521,6 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const float* part_o = reinterpret_cast<const float*>(ws + L.part_o);
-    const float* part_lse = reinterpret_cast<const float*>(ws + L.part_lse);
-    const int* slot_base = reinterpret_cast<const int*>(ws + L.slot_base);
     const cudaError_t e =
         per_head ? cudaLaunchKernelEx(&cfg, combine_heads_kernel, part_o, part_lse, slot_base, T,
                                       olat, ctx->status)
@@ -458,7 +530,7 @@ bool bf16_decode(mla_ctx* ctx, const __nv_bfloat16* q, const __nv_bfloat16* cach
       return false;
   }
   // ---- value up-projection: o_i = W^UV_i o_lat_i
-  {
+  if (!fused_uv) {
     WgPlan p{};
     p.nt = bp.uv.nt;
     p.n_tiles = bp.uv.n_tiles;
@@ -563,6 +635,31 @@ bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsL
     ctx->launches += 1;
     return check(wgemm_launch(p, WG_ROWMAJOR, false, st, true));
   };
+  if (M <= kGemvMaxTokens) {
+    // one or two tokens: matrix-vector products, bound by streaming the weights
+    auto gemv = [&](const void* W, int R, int K, const __nv_bfloat16* x, __nv_bfloat16* out,
+                    long long ldo, int rph, long long hs, const char* name) {
+      GemvArgs g{static_cast<const __nv_bfloat16*>(W), R, K, M, x, (long long)K, R, 0, out,
+                 ldo, rph, hs};
+      if (!gemv_supported(g, ctx->num_sms)) return false;
+      prof_mark(ctx, st, name);
+      ctx->launches += 1;
+      return check(gemv_launch(g, ctx->num_sms, st, true));
+    };
+    const GemvArgs probe_dq{nullptr, dcq, D, M, nullptr, D, dcq, 0, nullptr, dcq, 0, 0};
+    const GemvArgs probe_uq{nullptr, kHeads * kNope, dcq, M, nullptr, dcq, kHeads * kNope, 0,
+                            nullptr, kQRow, kNope, kNope + kRope};
+    const GemvArgs probe_qr{nullptr, kHeads * kRope, D, M, nullptr, D, kHeads * kRope, 0,
+                            nullptr, kQRow, kRope, kNope + kRope};
+    if (gemv_supported(probe_dq, ctx->num_sms) && gemv_supported(probe_uq, ctx->num_sms) &&
+        gemv_supported(probe_qr, ctx->num_sms)) {
+      return gemv(ctx->w.w_dq, dcq, D, h, cq, dcq, 0, 0, "query_down") &&
+             gemv(ctx->w.w_qr, kHeads * kRope, D, h, q + kNope, kQRow, kRope, kNope + kRope,
+                  "query_rope") &&
+             gemv(ctx->w.w_uq, kHeads * kNope, dcq, cq, q, kQRow, kNope, kNope + kRope,
+                  "query_up");
+    }
+  }
   // c^Q [M, d_cq]
   if (!rowmajor(bp.dq, dcq / 128, ctx->tm_wdq, h, D, D / 64, dcq / 128, 0, cq, dcq, 0, 0,
                 "query_down"))
@@ -631,7 +728,8 @@ bool bf16_append_decode(mla_ctx* ctx, const __nv_bfloat16* h, const int32_t* pos
                    p))
     return false;
   p.args.stage_rows = kv_fp8(ctx) ? 1 : 0;
-  return bf16_decode(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st, &p);
+  return decode_impl(ctx, q, cache, num_pages, bt, max_pages, seq_lens, B, T, out, ws, L, st, &p,
+                     h);
 }
 
 }  // namespace mla

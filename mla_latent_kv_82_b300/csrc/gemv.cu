@@ -20,6 +20,7 @@
 
 #include "device_util.cuh"
 #include "gemv.h"
+#include "tc_util.cuh"
 #include "launch_util.h"
 
 namespace mla {
@@ -64,7 +65,7 @@ template <int M>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const __nv_bfloat16* __restrict__ W, int R, int K, const __nv_bfloat16* __restrict__ x,
             long long ldx, int rows_per_seg, long long seg_stride, __nv_bfloat16* __restrict__ out,
-            long long ldo) {
+            long long ldo, int out_rph, long long out_hs) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* part = reinterpret_cast<float*>(smem + kSmemX);   // [row][seg][M]
   uint4* xs = reinterpret_cast<uint4*>(smem);               // [M][K / 8] (one x segment)
@@ -135,8 +136,207 @@ gemv_kernel(const __nv_bfloat16* __restrict__ W, int R, int K, const __nv_bfloat
     const int i = e / M, t = e % M;
     float v = 0.f;
     for (int sg = 0; sg < nseg; ++sg) v += part[(i * nseg + sg) * M + t];
-    out[t * ldo + r_lo + i] = __float2bfloat16_rn(v);
+    const int r = r_lo + i;
+    const long long col = out_rph > 0 ? (long long)(r / out_rph) * out_hs + r % out_rph : r;
+    out[t * ldo + col] = __float2bfloat16_rn(v);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp combine fused with the value up-projection, for one or two
+// query tokens: o_lat[m, h] = sum_s w_s O_s[m, h] / sum_s w_s (w_s = 2^(lse_s
+// - max), the splits of token m's sequence), rounded to bf16 as stored, then
+// o[m, h*128 + r] = W^UV[h*128 + r, :] . o_lat[m, h] (page "DeepSeek-V2：在
+// “大力出奇迹”的AI军备竞赛中，四两拨千斤", liang.world, 第二章 §2: the value
+// half of the absorbed form applies W^UV_i to the attention-weighted latent).
+//
+// One CTA per SM owns a contiguous range of at most 128 rows of W^UV (so at
+// most two heads).  Its rows are one contiguous block of memory, fetched by
+// bulk copies into shared memory before the kernel waits for the attention;
+// then the CTA merges the split results of its heads from L2 (thread = 4
+// columns x a subset of the splits, eight loads in flight, subsets added in
+// order), and each warp reduces its rows' dot products.  The CTA holding a
+// head's first row writes that head's o_lat.
+constexpr int kUvRows = 128;      // rows (and value features) per head
+constexpr int kUvK = 512;         // latent width
+constexpr int kUvMaxRows = 128;   // rows per CTA
+constexpr int kUvMaxPairs = kGemvMaxTokens * 2;   // (token, head) pairs per CTA
+constexpr int kUvMaxSlots = 256;  // splits per sequence
+constexpr int kUvLoads = 8;       // split results in flight per thread
+constexpr uint32_t kUvOffW = 0;                                    // weights [row][512]
+constexpr uint32_t kUvOffSl = kUvMaxRows * kUvK * 2;               // split weights [pair][slot]
+constexpr uint32_t kUvOffRed = kUvOffSl + kUvMaxPairs * kUvMaxSlots * 4;   // [thread] float4
+constexpr uint32_t kUvOffX = kUvOffRed + kThreads * 16;            // o_lat [pair][512] bf16
+constexpr uint32_t kUvOffSum = kUvOffX + kUvMaxPairs * kUvK * 2;   // [pair] float
+constexpr uint32_t kUvOffBar = kUvOffSum + kUvMaxPairs * 4;
+constexpr uint32_t kUvSmem = kUvOffBar + 16;
+static_assert(kUvSmem <= 232448 && kUvOffBar % 8 == 0, "shared memory");
+
+template <int M>
+__global__ void __launch_bounds__(kThreads, 1)
+combine_value_kernel(const __nv_bfloat16* __restrict__ W, int R, const float* __restrict__ part_o,
+                     const float* __restrict__ part_lse, const int* __restrict__ slot_base, int T,
+                     int n_heads, __nv_bfloat16* __restrict__ o_lat, __nv_bfloat16* __restrict__ out,
+                     int* status) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const uint4* wsm = reinterpret_cast<const uint4*>(smem + kUvOffW);
+  float* wsl = reinterpret_cast<float*>(smem + kUvOffSl);
+  float4* red = reinterpret_cast<float4*>(smem + kUvOffRed);
+  uint4* xs = reinterpret_cast<uint4*>(smem + kUvOffX);
+  float* wsum = reinterpret_cast<float*>(smem + kUvOffSum);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUvOffBar);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r_lo = (int)((long long)blockIdx.x * R / gridDim.x);
+  const int r_hi = (int)((long long)(blockIdx.x + 1) * R / gridDim.x);
+  const int h0 = r_lo / kUvRows;
+  const int nh = r_hi > r_lo ? (r_hi - 1) / kUvRows - h0 + 1 : 0;
+  const int np = M * nh;                  // (token, head) pairs, token-major
+
+  // this CTA's weight rows: independent of the previous kernel
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const uint32_t bytes = (uint32_t)(r_hi - r_lo) * kUvK * 2;
+    tc::mbar_arrive_expect_tx(smem_u32(bar), bytes);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(W + (size_t)r_lo * kUvK);
+    for (uint32_t o = 0; o < bytes; o += 32768)
+      tc::bulk_load(smem_u32(smem + kUvOffW + o), src + o, min(32768u, bytes - o), smem_u32(bar));
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the split results
+
+  // weights of the splits, one warp per pair
+  if (warp < np) {
+    const int m = warp / nh, head = h0 + warp % nh;
+    const int b = m / T, t = m % T;
+    const int s0 = slot_base[b];
+    int n = slot_base[b + 1] - s0;
+    if (n > kUvMaxSlots) {   // cannot happen with the planner's split counts
+      if (lane == 0) report(status, MLA_ERR_INVALID_ARG, 61);
+      n = kUvMaxSlots;
+    }
+    float* wp = wsl + warp * kUvMaxSlots;
+    float lmax = -INFINITY;
+    for (int i = lane; i < n; i += 32) {
+      const float v = part_lse[((size_t)(s0 + i) * T + t) * n_heads + head];
+      wp[i] = v;
+      lmax = fmaxf(lmax, v);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) wp[i] = exp2f(wp[i] - lmax);
+    __syncwarp();
+    if (lane == 0) {   // in slot order
+      float s = 0.f;
+      for (int i = 0; i < n; ++i) s += wp[i];
+      wsum[warp] = s;
+    }
+  }
+  __syncthreads();
+
+  // merge: thread = (pair, subset of the splits, 4 columns)
+  const int subs = kThreads / (np * 128);
+  const int pr = tid / (subs * 128), sub = (tid / 128) % subs, c4 = tid % 128;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (pr < np) {
+    const int m = pr / nh, head = h0 + pr % nh;
+    const int b = m / T, t = m % T;
+    const int s0 = slot_base[b];
+    const int n = min(slot_base[b + 1] - s0, kUvMaxSlots);
+    if (n > 1) {
+      const float* wp = wsl + pr * kUvMaxSlots;
+      const float4* src = reinterpret_cast<const float4*>(part_o) + c4;
+      const size_t stride = (size_t)T * n_heads * (kUvK / 4);   // float4s between slots
+      const size_t base = ((size_t)s0 * T + t) * n_heads * (kUvK / 4) + (size_t)head * (kUvK / 4);
+      for (int i0 = sub; i0 < n; i0 += kUvLoads * subs) {
+        float4 x[kUvLoads];
+        float ws[kUvLoads];
+#pragma unroll
+        for (int j = 0; j < kUvLoads; ++j) {
+          const int i = i0 + j * subs;
+          ws[j] = i < n ? wp[i] : 0.f;
+          // an empty split (no visible token) has weight 0 and no result
+          x[j] = ws[j] != 0.f ? __ldcg(src + base + (size_t)i * stride)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kUvLoads; ++j) {
+          acc.x = fmaf(ws[j], x[j].x, acc.x);
+          acc.y = fmaf(ws[j], x[j].y, acc.y);
+          acc.z = fmaf(ws[j], x[j].z, acc.z);
+          acc.w = fmaf(ws[j], x[j].w, acc.w);
+        }
+      }
+    }
+  }
+  red[tid] = acc;
+  __syncthreads();
+  if (tid < np * 128) {
+    const int p = tid / 128, c = tid % 128;
+    const int m = p / nh, head = h0 + p % nh;
+    const int b = m / T;
+    const int n = slot_base[b + 1] - slot_base[b];
+    __nv_bfloat16* dst = o_lat + ((size_t)m * n_heads + head) * kUvK + c * 4;
+    uint2 v;
+    if (n > 1) {
+      float4 a = red[p * subs * 128 + c];
+      for (int s = 1; s < subs; ++s) {
+        const float4 y = red[(p * subs + s) * 128 + c];
+        a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
+      }
+      const float inv = 1.f / wsum[p];
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+      v.x = *reinterpret_cast<const uint32_t*>(&lo);
+      v.y = *reinterpret_cast<const uint32_t*>(&hi);
+      if (head * kUvRows >= r_lo) *reinterpret_cast<uint2*>(dst) = v;   // the head's first row is here
+    } else {
+      // one split held the whole sequence: it wrote o_lat itself
+      v = __ldcg(reinterpret_cast<const uint2*>(dst));
+    }
+    reinterpret_cast<uint2*>(xs)[p * (kUvK / 4) + c] = v;
+  }
+  __syncthreads();
+  if (!mbar_wait(bar, 0, status, 62)) return;
+
+  // o = W^UV o_lat: a warp per row, two chunks of 8 columns per lane
+  for (int row = r_lo + warp; row < r_hi; row += kWarps) {
+    const int hl = row / kUvRows - h0;
+    const uint4* wr = wsm + (size_t)(row - r_lo) * (kUvK / 8);
+    const uint4 w0 = wr[lane], w1 = wr[lane + 32];
+    float acc_t[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+      acc_t[t] = 0.f;
+      fma8(acc_t[t], w0, xs[(t * nh + hl) * (kUvK / 8) + lane]);
+      fma8(acc_t[t], w1, xs[(t * nh + hl) * (kUvK / 8) + lane + 32]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc_t[t] += __shfl_xor_sync(0xffffffffu, acc_t[t], o);
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int t = 0; t < M; ++t) out[(size_t)t * R + row] = __float2bfloat16_rn(acc_t[t]);
+  }
+}
+
+template <int M>
+cudaError_t launch_uv(const CombineValueArgs& g, int ctas, cudaStream_t st) {
+  auto kern = combine_value_kernel<M>;
+  static std::atomic<uint64_t> attr_done{0};   // per instantiation
+  if (const cudaError_t e = smem_attr_once(attr_done, kern, (int)kUvSmem); e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kUvSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, g.W, g.n_heads * kUvRows, g.part_o, g.part_lse,
+                            g.slot_base, g.T, g.n_heads, g.o_lat, g.out, g.status);
 }
 
 template <int M>
@@ -155,7 +355,7 @@ cudaError_t launch_m(const GemvArgs& g, int ctas, cudaStream_t st, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, g.W, g.R, g.K, g.x, g.ldx, g.rows_per_seg, g.seg_stride,
-                            g.out, g.ldo);
+                            g.out, g.ldo, g.out_rows_per_head, g.out_head_stride);
 }
 
 }  // namespace
@@ -169,6 +369,17 @@ bool gemv_supported(const GemvArgs& g, int num_sms) {
 cudaError_t gemv_launch(const GemvArgs& g, int num_sms, cudaStream_t st, bool pdl) {
   if (!gemv_supported(g, num_sms)) return cudaErrorInvalidValue;
   return g.M == 1 ? launch_m<1>(g, num_sms, st, pdl) : launch_m<2>(g, num_sms, st, pdl);
+}
+
+bool combine_value_supported(const CombineValueArgs& g, int num_sms) {
+  const int R = g.n_heads * kUvRows;
+  return g.M >= 1 && g.M <= kGemvMaxTokens && g.T >= 1 && g.M % g.T == 0 && R >= num_sms &&
+         (R + num_sms - 1) / num_sms <= kUvMaxRows && g.max_slots <= kUvMaxSlots;
+}
+
+cudaError_t combine_value_launch(const CombineValueArgs& g, int num_sms, cudaStream_t st) {
+  if (!combine_value_supported(g, num_sms)) return cudaErrorInvalidValue;
+  return g.M == 1 ? launch_uv<1>(g, num_sms, st) : launch_uv<2>(g, num_sms, st);
 }
 
 }  // namespace mla

@@ -219,8 +219,8 @@ def run_sv_protocol(segs, pair: bool, rescale: bool, seed: int | None, drop: str
             n = ntiles(p0, p1)
             if k > 0 and "q_empty" not in drop:
                 yield q_empty[x], k - 1
+            qc[x] = k          # q~ into TMEM while the RoPE block lands
             yield qr[x], k
-            qc[x] = k
             q_ready.arrive()
             for i in range(n):
                 yield s_full[x][g & 1], g >> 1

@@ -111,6 +111,8 @@ def _compare(st, seqs=None, exact_too=False):
     (2, [0, 62, 63, 127, 500]),
     (3, [2, 64, 190]),
     (1, [300]),
+    (2, [200]),
+    (1, [70, 1]),
     (4, [3, 130, 260]),
 ])
 def test_small_fp8(T, lens):

@@ -152,6 +152,8 @@ def test_bad_page_id_is_reported_not_written():
     lambda: tiny_f32([5, 40, 64], 1),
     lambda: small_bf16([0, 63, 200, 1000], 1),
     lambda: small_bf16([62, 127, 500], 2),
+    lambda: small_bf16([200], 2),       # two tokens of one sequence (CUDA-core projections)
+    lambda: small_bf16([70, 1], 1),     # two sequences of one token
     lambda: W.config("b1-l4096"),
 ])
 def test_append_decode_equals_two_calls(make):
