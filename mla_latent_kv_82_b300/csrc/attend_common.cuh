@@ -34,6 +34,7 @@ struct AttArgs {
   float scale_log2;
 };
 
+
 // Iterates the (sequence, page range) segments of split c, in order.
 struct SegIter {
   const AttArgs* a;
@@ -196,110 +197,6 @@ struct RingPos {
     for (int j = 0; j < m; ++j) next();
   }
 };
-
-// Softmax warps (thread = head, warp w reads TMEM lanes 32 (w % 4)..): for
-// each tile of each segment of split c, wait for S, take the row maximum and
-// P = 2^(s * scale - m) in the log2 domain with a lazy rescale (O and l are
-// rescaled only when the maximum grows by more than 2^kRescale, so P <= 256),
-// write P as packed bf16 over the S columns and signal arrive_p(g); at the
-// end of a segment write O / l and m + log2 l for the log-sum-exp combine
-// and signal arrive_o().  s0/s1 and pv0/pv1 are the barriers of even and odd
-// tiles.  Tiles are those of token t_iter's range (what the MMA issuers
-// iterate); scores past token t's own causal end are masked.  On a failed
-// wait the CTA's abort flag is set.
-template <bool kCluster, class ArriveP, class ArriveO>
-__device__ __forceinline__ void softmax_role(const AttArgs& a, uint32_t tmem, int warp, int lane,
-                                             int c, int t, int t_iter, int half, uint64_t* s0,
-                                             uint64_t* s1, uint64_t* pv0, uint64_t* pv1,
-                                             volatile int* abort_flag, ArriveP arrive_p,
-                                             ArriveO arrive_o) {
-  const int q4 = warp & 3;
-  const int row = q4 * 32 + lane;          // head
-  const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-  SegIter it;
-  it.init(&a, c, t_iter);   // tiles as the MMA issuers see them
-  int sb, p0, p1, slot, g = 0;
-  bool ok = true;
-  while (ok && it.next(&sb, &p0, &p1, &slot)) {
-    const int n = ntiles_of(p0, p1);
-    // this token's own causal end (t_iter may see one more token)
-    const int p1_own = min(p1, a.lens[sb] - a.T + t + 1);
-    const size_t prow = ((size_t)slot * a.T + t) * kHeads + row;
-    float* dst = a.part_o + prow * kLat + half * 256;
-    if (n == 0) {
-      for (int j = 0; j < 256; j += 4)
-        *reinterpret_cast<float4*>(dst + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (half == 0) a.part_lse[prow] = -INFINITY;
-      continue;
-    }
-    float m_used = -INFINITY, l = 0.f;
-    for (int i = 0; i < n; ++i, ++g) {
-      const uint32_t scol = trow + kColS + (g & 1) * kTile;
-      ok = bar_wait<kCluster>((g & 1) ? s1 : s0, (g >> 1) & 1, a.status, 27);
-      if (__any_sync(0xffffffffu, !ok || *abort_flag)) { ok = false; break; }
-      tc::fence_after_sync();
-      const int valid = max(0, min(kTile, p1_own - (p0 + i * kTile)));
-      // the whole S row of this tile (128 tokens) into registers
-      uint32_t lo[64], hi[64];
-      tc::tmem_ld64(scol, lo);
-      tc::tmem_ld64(scol + 64, hi);
-      float mx = valid == kTile ? row_max<false>(lo, hi, valid) : row_max<true>(lo, hi, valid);
-      mx *= a.scale_log2;
-      // S(g) done implies every earlier value MMA but PV(g-1) is done, so
-      // P(g) may overwrite S(g) now; only a rescale of O waits for PV(g-1).
-      const bool need = mx > m_used + kRescale;
-      if (i == 0) {
-        m_used = mx;
-      } else if (__any_sync(0xffffffffu, need)) {
-        ok = bar_wait<kCluster>(((g - 1) & 1) ? pv1 : pv0, ((g - 1) >> 1) & 1, a.status, 28);
-        if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-        tc::fence_after_sync();
-        const float m_new = need ? mx : m_used;
-        const float f = exp2f(m_used - m_new);
-        l *= f;
-        for (int c0 = 0; c0 < 256; c0 += 16) {
-          float v[16];
-          tc::tmem_ld16(trow + c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] *= f;
-          tc::tmem_st16(trow + c0, v);
-        }
-        m_used = m_new;
-      }
-      // P = 2^(s*scale - m) as bf16, packed two per column over the S
-      // columns (tokens 2j, 2j+1 -> column j)
-      uint32_t pk[64];
-      const float psum = valid == kTile
-                             ? exp_pack<false>(lo, hi, valid, a.scale_log2, m_used, pk)
-                             : exp_pack<true>(lo, hi, valid, a.scale_log2, m_used, pk);
-      tc::tmem_st64(scol, pk);
-      l += psum;
-      tc::fence_before_sync();
-      arrive_p(g);
-    }
-    if (!ok) break;
-    // segment epilogue: O / l and the log-sum-exp
-    // PV of the last tile done implies every earlier one is
-    ok = bar_wait<kCluster>(((g - 1) & 1) ? pv1 : pv0, ((g - 1) >> 1) & 1, a.status, 29);
-    if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-    tc::fence_after_sync();
-    // l = 0 only when this token sees none of the segment's tokens (P >= 1
-    // at the row maximum otherwise): an empty partial
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int c0 = 0; c0 < 256; c0 += 16) {
-      float v[16];
-      tc::tmem_ld16(trow + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        __stcg(reinterpret_cast<float4*>(dst + c0 + j),
-               make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
-    }
-    if (half == 0) a.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
-    tc::fence_before_sync();
-    arrive_o();
-  }
-  if (!ok) *abort_flag = 1;
-}
 
 }  // namespace att
 }  // namespace mla

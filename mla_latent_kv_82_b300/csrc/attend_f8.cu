@@ -426,19 +426,18 @@ attend_f8_kernel(const __grid_constant__ CUtensorMap tmB,   // pool, box {128 B,
     bool ok = true;
     while (ok && it.next(&sb, &p0, &p1, &slot)) {
       const int n = ntiles_of(p0, p1);
-      const size_t prow = ((size_t)slot * a.T + t) * kHeads + row;
+      const size_t st_idx = (size_t)slot * a.T + t;   // (slot, token) of the split result
+      const size_t prow = st_idx * kHeads + row;
       // one split holds the whole sequence: write o_lat here, no combine
       const bool direct = a.slot_base[sb + 1] - a.slot_base[sb] == 1;
       __nv_bfloat16* olat =
           a.o_lat + (((size_t)sb * a.T + t) * kHeads + row) * kLat + half * 256;
-      float* dst = a.part_o + prow * kLat + half * 256;
+      float* dst = a.part_o + part_off(st_idx, row, half * 256);   // chunk j at + j * 128
       if (n == 0) {
+        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         for (int j = 0; j < 256; j += 8) {
           if (direct) *reinterpret_cast<uint4*>(olat + j) = make_uint4(0u, 0u, 0u, 0u);
-          else {
-            *reinterpret_cast<float4*>(dst + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(dst + j + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          else st_v8(dst + (size_t)(j >> 3) * 128, z);
         }
         if (!direct && half == 0) a.part_lse[prow] = -INFINITY;
         continue;
@@ -520,9 +519,12 @@ attend_f8_kernel(const __grid_constant__ CUtensorMap tmB,   // pool, box {128 B,
           *reinterpret_cast<uint4*>(olat + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            __stcg(reinterpret_cast<float4*>(dst + c0 + j),
-                   make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv));
+          for (int j = 0; j < 16; j += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[j + e] * inv);
+            st_v8(dst + (size_t)((c0 + j) >> 3) * 128, w);
+          }
         }
       }
       if (!direct && half == 0) a.part_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;

@@ -100,14 +100,6 @@ enum : int {
   kBSlot = 50      // TMEM base address (u32) and abort flag (u32)
 };
 
-// One 32-byte store (a whole L2 sector per thread: the epilogue writes a
-// row per thread, so 16-byte stores would fill half of each sector).
-__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.cg.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
-               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
-
 constexpr uint32_t kColQ = 0;     // score: q~ (256 columns)
 constexpr uint32_t kColS = 256;   // score: S buffers at 256 and 384
 
@@ -428,28 +420,21 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
       if (!fail && k > 0) fail = !cwait<kPair>(&bar[kBQEmpty], (k - 1) & 1, a.status, 76);
       if (!fail) {
         tc::fence_after_sync();
-        const uint8_t* img = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes + prow_off;
-        // two rounds of four feature blocks, 32 loads in flight per thread
+        // chunk-major image: 32-byte chunk J of this head at J * 4096 +
+        // row * 32, so the warp's 32 heads read 1 KB contiguous per load
+        const uint8_t* img = a.qimg + ((size_t)sb * a.T + t) * kQImgBytes + row * 32;
+        // two rounds of four feature blocks (four chunks each), 16 loads of
+        // 32 bytes in flight per thread
 #pragma unroll 1
         for (int f0 = 0; f0 < 8; f0 += 4) {
-          uint4 v[4][8];
+          uint32_t v[4][32];
 #pragma unroll
           for (int fb = 0; fb < 4; ++fb)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              v[fb][j] = tc::ld_nc_v4(img + (f0 + fb) * 16384 + ((j ^ (row & 7)) << 4));
+            for (int j = 0; j < 4; ++j)
+              ld_nc_v8(img + ((f0 + fb) * 4 + j) * 4096, &v[fb][8 * j]);
 #pragma unroll
-          for (int fb = 0; fb < 4; ++fb) {
-            uint32_t w[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              w[4 * j] = v[fb][j].x;
-              w[4 * j + 1] = v[fb][j].y;
-              w[4 * j + 2] = v[fb][j].z;
-              w[4 * j + 3] = v[fb][j].w;
-            }
-            tc::tmem_st32(trow + kColQ + (f0 + fb) * 32, w);
-          }
+          for (int fb = 0; fb < 4; ++fb) tc::tmem_st32(trow + kColQ + (f0 + fb) * 32, v[fb]);
         }
         tc::fence_before_sync();
         // the RoPE block lands in parallel; q~ and it are ready together
@@ -697,11 +682,11 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
     bool ok = true;
     while (ok && it.next(&sb, &p0, &p1, &slot)) {
       const int n = ntiles_of(p0, p1);
-      const size_t prow = ((size_t)slot * a.T + t) * kHeads + row;
-      float* dst = a.part_o + prow * kLat;
+      const size_t st_idx = (size_t)slot * a.T + t;   // (slot, token) of the split result
+      float* dst = a.part_o + part_off(st_idx, row, 0);   // chunk j at + j * 128
       if (n == 0) {
-        for (int j = 0; j < kLat; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        for (int j = 0; j < kLat / 8; ++j) st_v8(dst + (size_t)j * 128, z);
         continue;
       }
       float l = 0.f;
@@ -771,7 +756,7 @@ attend_sv_kernel(const __grid_constant__ CUtensorMap tmS,    // pool, box {64, 6
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[j + e]) * inv);
-            st_v8(dst + c0 + j, w);
+            st_v8(dst + (size_t)((c0 + j) >> 3) * 128, w);
           }
         }
       }

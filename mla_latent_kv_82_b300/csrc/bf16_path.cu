@@ -21,11 +21,13 @@ namespace {
 // flash-decoding.  A sequence held by one split alone is skipped: the
 // attention kernel wrote its o_lat directly.  For sequences cut into many splits (a few long
 // sequences), one CTA per (token, head): the split weights are formed
-// once in shared memory, then two groups of 128 threads (one float4 of the
-// 512 latent columns per thread) each sum every other split with eight
-// independent loads in flight, and the two sums are added in a fixed order.
+// once in shared memory, then four groups of 64 threads (one 8-column chunk
+// of the 512 latent columns per thread, 32-byte loads) each sum every fourth
+// split with eight independent loads in flight, and the four sums are added
+// in a fixed order.
 constexpr int kCombineThreads = 256;
 constexpr int kCombineMaxSlots = 1024;
+constexpr int kCombineGroups = kCombineThreads / (kLat / 8);   // 4
 
 __global__ void __launch_bounds__(kCombineThreads)
 combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
@@ -33,7 +35,7 @@ combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__
                      int* status) {
   __shared__ float w[kCombineMaxSlots];
   __shared__ float red[2];
-  __shared__ float4 acc1[kLat / 4];
+  __shared__ float acc1[kCombineGroups - 1][kLat];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int mh = blockIdx.x;                   // token row * kHeads + head
@@ -68,46 +70,55 @@ combine_heads_kernel(const float* __restrict__ part_o, const float* __restrict__
     for (int i = 0; i < n; ++i) sum += w[i];
     red[0] = sum;
   }
-  const int g = tid >> 7, q4 = tid & 127;
-  const float4* src = reinterpret_cast<const float4*>(part_o) + q4;
-  const size_t stride = (size_t)T * kHeads * (kLat / 4);   // float4s between slots
-  const size_t base = ((size_t)s0 * T + t) * kHeads * (kLat / 4) + (size_t)head * (kLat / 4);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = g; i0 < n; i0 += 16) {
-    float4 x[8];
+  const int g = tid / (kLat / 8), c8 = tid % (kLat / 8);
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  for (int i0 = g; i0 < n; i0 += 8 * kCombineGroups) {
+    float x[8][8];
     float ws[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int i = i0 + 2 * j;
+      const int i = i0 + kCombineGroups * j;
       ws[j] = i < n ? w[i] : 0.f;
-      x[j] = ws[j] != 0.f ? __ldcg(src + base + (size_t)i * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ws[j] != 0.f) {
+        ld_cg_v8(part_o + part_off((size_t)(s0 + i) * T + t, head, c8 * 8), x[j]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[j][e] = 0.f;
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      acc.x = fmaf(ws[j], x[j].x, acc.x);
-      acc.y = fmaf(ws[j], x[j].y, acc.y);
-      acc.z = fmaf(ws[j], x[j].z, acc.z);
-      acc.w = fmaf(ws[j], x[j].w, acc.w);
-    }
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws[j], x[j][e], acc[e]);
   }
-  if (g == 1) acc1[q4] = acc;
+  if (g > 0)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc1[g - 1][c8 * 8 + e] = acc[e];
   __syncthreads();
-  if (g == 1) return;
-  const float4 y = acc1[q4];
+  if (g > 0) return;
   const float inv = 1.f / red[0];
-  const __nv_bfloat162 lo = __floats2bfloat162_rn((acc.x + y.x) * inv, (acc.y + y.y) * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn((acc.z + y.z) * inv, (acc.w + y.w) * inv);
-  uint2 v;
-  v.x = *reinterpret_cast<const uint32_t*>(&lo);
-  v.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(o_lat + (size_t)mh * kLat + q4 * 4) = v;
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    float a0 = acc[e], a1 = acc[e + 1];
+#pragma unroll
+    for (int gg = 0; gg < kCombineGroups - 1; ++gg) {
+      a0 += acc1[gg][c8 * 8 + e];
+      a1 += acc1[gg][c8 * 8 + e + 1];
+    }
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+    o[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  *reinterpret_cast<uint4*>(o_lat + (size_t)mh * kLat + c8 * 8) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // The same merge for sequences split into a few pieces only: one CTA per
 // (token, 16 heads), so that a token whose sequence one split held (it wrote
 // o_lat itself) costs one small CTA that leaves at once; a thread takes one
-// head and 8 runs of 4 latent columns, with the 8 loads of a split in flight
-// together (coalesced 256-byte runs per half warp).
+// head and four 8-column chunks (32-byte loads, the four of a split in flight
+// together; the 16 heads of a chunk are 512 contiguous bytes).
 constexpr int kCombineHeads = 16;
 __global__ void __launch_bounds__(256)
 combine_rows_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
@@ -115,45 +126,50 @@ combine_rows_kernel(const float* __restrict__ part_o, const float* __restrict__ 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int m = blockIdx.x / (kHeads / kCombineHeads);
-  const int head = (blockIdx.x % (kHeads / kCombineHeads)) * kCombineHeads + threadIdx.x / 16;
-  const int c4 = threadIdx.x % 16;   // runs c4, c4 + 16, ... of 4 columns
+  const int head = (blockIdx.x % (kHeads / kCombineHeads)) * kCombineHeads + threadIdx.x % 16;
+  const int part = threadIdx.x / 16;   // chunks part * 4 .. part * 4 + 3
   const int b = m / T, t = m % T;
   const int s0 = slot_base[b], s1 = slot_base[b + 1];
   if (s1 - s0 == 1) return;   // one split held the whole sequence: it wrote o_lat itself
   float lmax = -INFINITY;
   for (int s = s0; s < s1; ++s) lmax = fmaxf(lmax, part_lse[((size_t)s * T + t) * kHeads + head]);
-  float4 acc[8];
+  float acc[4][8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
   float wsum = 0.f;
   for (int s = s0; s < s1; ++s) {
-    const size_t r = ((size_t)s * T + t) * kHeads + head;
-    const float w = exp2f(part_lse[r] - lmax);
+    const size_t st = (size_t)s * T + t;
+    const float w = exp2f(part_lse[st * kHeads + head] - lmax);
     wsum += w;
     if (w == 0.f) continue;   // an empty split (no visible token) contributes nothing
-    const float4* src = reinterpret_cast<const float4*>(part_o + r * kLat) + c4;
-    float4 x[8];
+    float x[4][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = __ldcg(src + 16 * j);
+    for (int j = 0; j < 4; ++j) ld_cg_v8(part_o + part_off(st, head, (part * 4 + j) * 8), x[j]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      acc[j].x = fmaf(w, x[j].x, acc[j].x);
-      acc[j].y = fmaf(w, x[j].y, acc[j].y);
-      acc[j].z = fmaf(w, x[j].z, acc[j].z);
-      acc[j].w = fmaf(w, x[j].w, acc[j].w);
-    }
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(w, x[j][e], acc[j][e]);
   }
+  // the 16 heads' rows (16 KB of o_lat, contiguous) staged in shared memory,
+  // then stored 16 bytes per thread in address order
+  __shared__ uint4 stage[kCombineHeads * kLat / 8];
   const float inv = 1.f / wsum;
-  __nv_bfloat16* dst = o_lat + ((size_t)m * kHeads + head) * kLat + c4 * 4;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
-    uint2 v;
-    v.x = *reinterpret_cast<const uint32_t*>(&lo);
-    v.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst + 64 * j) = v;
+  for (int j = 0; j < 4; ++j) {
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[j][e] * inv, acc[j][e + 1] * inv);
+      o[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    stage[(threadIdx.x % 16) * (kLat / 8) + part * 4 + j] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(o_lat + ((size_t)m * kHeads + head - threadIdx.x % 16) * kLat);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) dst[threadIdx.x + 256 * j] = stage[threadIdx.x + 256 * j];
 }
 
 // K splits so that one wave fills the SMs, within the scratch budget.

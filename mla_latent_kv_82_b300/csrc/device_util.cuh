@@ -118,6 +118,47 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from global to
+// shared memory with 16-byte asynchronous copies strided over `nthreads`
+// threads (each thread's share; complete with cp_async_wait_all and a block
+// barrier).  Many independent requests per thread keep the copy near the
+// HBM rate without holding registers.
+__device__ __forceinline__ void cp_async_block(void* dst, const void* src, size_t bytes, int tid,
+                                               int nthreads) {
+  const uint32_t d = smem_u32(dst);
+  const char* s = static_cast<const char*>(src);
+  for (size_t o = (size_t)tid * 16; o < bytes; o += (size_t)nthreads * 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + (uint32_t)o), "l"(s + o)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+
+// 32-byte global accesses (a whole L2 sector per thread), caching in L2
+// only: the split results are written and read 8 fp32 columns at a time.
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.cg.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// 32 bytes of read-only data through the non-coherent path.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t* v) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void ld_cg_v8(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                 "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f(float x);

@@ -20,6 +20,7 @@
 
 #include "device_util.cuh"
 #include "gemv.h"
+#include "layouts.cuh"
 #include "tc_util.cuh"
 #include "launch_util.h"
 
@@ -151,8 +152,9 @@ gemv_kernel(const __nv_bfloat16* __restrict__ W, int R, int K, const __nv_bfloat
 // half of the absorbed form applies W^UV_i to the attention-weighted latent).
 //
 // One CTA per SM owns a contiguous range of at most 128 rows of W^UV (so at
-// most two heads).  Its rows are one contiguous block of memory, fetched by
-// bulk copies into shared memory before the kernel waits for the attention;
+// most two heads).  Its rows are one contiguous block of memory, fetched
+// with 16-byte asynchronous copies into shared memory before the kernel
+// waits for the attention;
 // then the CTA merges the split results of its heads from L2 (thread = 4
 // columns x a subset of the splits, eight loads in flight, subsets added in
 // order), and each warp reduces its rows' dot products.  The CTA holding a
@@ -165,8 +167,8 @@ constexpr int kUvMaxSlots = 256;  // splits per sequence
 constexpr int kUvLoads = 8;       // split results in flight per thread
 constexpr uint32_t kUvOffW = 0;                                    // weights [row][512]
 constexpr uint32_t kUvOffSl = kUvMaxRows * kUvK * 2;               // split weights [pair][slot]
-constexpr uint32_t kUvOffRed = kUvOffSl + kUvMaxPairs * kUvMaxSlots * 4;   // [thread] float4
-constexpr uint32_t kUvOffX = kUvOffRed + kThreads * 16;            // o_lat [pair][512] bf16
+constexpr uint32_t kUvOffRed = kUvOffSl + kUvMaxPairs * kUvMaxSlots * 4;   // [thread][8] fp32
+constexpr uint32_t kUvOffX = kUvOffRed + kThreads * 32;            // o_lat [pair][512] bf16
 constexpr uint32_t kUvOffSum = kUvOffX + kUvMaxPairs * kUvK * 2;   // [pair] float
 constexpr uint32_t kUvOffBar = kUvOffSum + kUvMaxPairs * 4;
 constexpr uint32_t kUvSmem = kUvOffBar + 16;
@@ -184,7 +186,6 @@ combine_value_kernel(const __nv_bfloat16* __restrict__ W, int R, const float* __
   float4* red = reinterpret_cast<float4*>(smem + kUvOffRed);
   uint4* xs = reinterpret_cast<uint4*>(smem + kUvOffX);
   float* wsum = reinterpret_cast<float*>(smem + kUvOffSum);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUvOffBar);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r_lo = (int)((long long)blockIdx.x * R / gridDim.x);
@@ -194,15 +195,8 @@ combine_value_kernel(const __nv_bfloat16* __restrict__ W, int R, const float* __
   const int np = M * nh;                  // (token, head) pairs, token-major
 
   // this CTA's weight rows: independent of the previous kernel
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const uint32_t bytes = (uint32_t)(r_hi - r_lo) * kUvK * 2;
-    tc::mbar_arrive_expect_tx(smem_u32(bar), bytes);
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(W + (size_t)r_lo * kUvK);
-    for (uint32_t o = 0; o < bytes; o += 32768)
-      tc::bulk_load(smem_u32(smem + kUvOffW + o), src + o, min(32768u, bytes - o), smem_u32(bar));
-  }
+  cp_async_block(smem + kUvOffW, W + (size_t)r_lo * kUvK, (size_t)(r_hi - r_lo) * kUvK * 2, tid,
+                 kThreads);
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the split results
 
   // weights of the splits, one warp per pair
@@ -235,10 +229,12 @@ combine_value_kernel(const __nv_bfloat16* __restrict__ W, int R, const float* __
   }
   __syncthreads();
 
-  // merge: thread = (pair, subset of the splits, 4 columns)
-  const int subs = kThreads / (np * 128);
-  const int pr = tid / (subs * 128), sub = (tid / 128) % subs, c4 = tid % 128;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // merge: thread = (pair, subset of the splits, 8-column chunk)
+  const int subs = kThreads / (np * 64);
+  const int pr = tid / (subs * 64), sub = (tid / 64) % subs, c8 = tid % 64;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   if (pr < np) {
     const int m = pr / nh, head = h0 + pr % nh;
     const int b = m / T, t = m % T;
@@ -246,59 +242,66 @@ combine_value_kernel(const __nv_bfloat16* __restrict__ W, int R, const float* __
     const int n = min(slot_base[b + 1] - s0, kUvMaxSlots);
     if (n > 1) {
       const float* wp = wsl + pr * kUvMaxSlots;
-      const float4* src = reinterpret_cast<const float4*>(part_o) + c4;
-      const size_t stride = (size_t)T * n_heads * (kUvK / 4);   // float4s between slots
-      const size_t base = ((size_t)s0 * T + t) * n_heads * (kUvK / 4) + (size_t)head * (kUvK / 4);
       for (int i0 = sub; i0 < n; i0 += kUvLoads * subs) {
-        float4 x[kUvLoads];
+        float x[kUvLoads][8];
         float ws[kUvLoads];
 #pragma unroll
         for (int j = 0; j < kUvLoads; ++j) {
           const int i = i0 + j * subs;
           ws[j] = i < n ? wp[i] : 0.f;
           // an empty split (no visible token) has weight 0 and no result
-          x[j] = ws[j] != 0.f ? __ldcg(src + base + (size_t)i * stride)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ws[j] != 0.f) {
+            ld_cg_v8(part_o + part_off((size_t)(s0 + i) * T + t, head, c8 * 8), x[j]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[j][e] = 0.f;
+          }
         }
 #pragma unroll
-        for (int j = 0; j < kUvLoads; ++j) {
-          acc.x = fmaf(ws[j], x[j].x, acc.x);
-          acc.y = fmaf(ws[j], x[j].y, acc.y);
-          acc.z = fmaf(ws[j], x[j].z, acc.z);
-          acc.w = fmaf(ws[j], x[j].w, acc.w);
-        }
+        for (int j = 0; j < kUvLoads; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] = fmaf(ws[j], x[j][e], acc[e]);
       }
     }
   }
-  red[tid] = acc;
+  float4* red4 = reinterpret_cast<float4*>(red);
+  red4[2 * tid] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  red4[2 * tid + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   __syncthreads();
-  if (tid < np * 128) {
-    const int p = tid / 128, c = tid % 128;
+  if (tid < np * 64) {
+    const int p = tid / 64, c = tid % 64;
     const int m = p / nh, head = h0 + p % nh;
     const int b = m / T;
     const int n = slot_base[b + 1] - slot_base[b];
-    __nv_bfloat16* dst = o_lat + ((size_t)m * n_heads + head) * kUvK + c * 4;
-    uint2 v;
+    __nv_bfloat16* dst = o_lat + ((size_t)m * n_heads + head) * kUvK + c * 8;
+    uint4 v;
     if (n > 1) {
-      float4 a = red[p * subs * 128 + c];
-      for (int s = 1; s < subs; ++s) {
-        const float4 y = red[(p * subs + s) * 128 + c];
-        a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
+      float a[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] = 0.f;
+      for (int sb = 0; sb < subs; ++sb) {   // the subsets in order
+        const int u = (p * subs + sb) * 64 + c;
+        const float4 y0 = red4[2 * u], y1 = red4[2 * u + 1];
+        a[0] += y0.x; a[1] += y0.y; a[2] += y0.z; a[3] += y0.w;
+        a[4] += y1.x; a[5] += y1.y; a[6] += y1.z; a[7] += y1.w;
       }
       const float inv = 1.f / wsum[p];
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-      v.x = *reinterpret_cast<const uint32_t*>(&lo);
-      v.y = *reinterpret_cast<const uint32_t*>(&hi);
-      if (head * kUvRows >= r_lo) *reinterpret_cast<uint2*>(dst) = v;   // the head's first row is here
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a[e] * inv, a[e + 1] * inv);
+        o[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      v = make_uint4(o[0], o[1], o[2], o[3]);
+      if (head * kUvRows >= r_lo) *reinterpret_cast<uint4*>(dst) = v;   // the head's first row is here
     } else {
       // one split held the whole sequence: it wrote o_lat itself
-      v = __ldcg(reinterpret_cast<const uint2*>(dst));
+      v = __ldcg(reinterpret_cast<const uint4*>(dst));
     }
-    reinterpret_cast<uint2*>(xs)[p * (kUvK / 4) + c] = v;
+    xs[p * (kUvK / 8) + c] = v;
   }
+  cp_async_wait_all();
   __syncthreads();
-  if (!mbar_wait(bar, 0, status, 62)) return;
 
   // o = W^UV o_lat: a warp per row, two chunks of 8 columns per lane
   for (int row = r_lo + warp; row < r_hi; row += kWarps) {

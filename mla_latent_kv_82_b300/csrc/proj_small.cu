@@ -11,8 +11,9 @@
 // 5.6 MB at V2 widths).  One CTA per SM: when the absorbed query is computed
 // CTA i < 128 owns head i's W^UK block (128 x 512, contiguous) and a few
 // rows of [W^DKV; W^KR]; the other CTAs share the remaining rows.  Each CTA
-// fetches its weights into shared memory with bulk copies before it waits
-// for the previous kernel (h and q may come from it), then computes:
+// fetches its weights into shared memory with 16-byte asynchronous copies
+// (many in flight per thread) before it waits for the previous kernel (h and
+// q may come from it), then computes:
 //   * W^UK_i^T q^C_i: eight warps, 16 weight rows each, lane = 16 latent
 //     columns; the eight partial sums added in warp order;
 //   * a row of [W^DKV; W^KR] . h: the row is cut into 8 fixed K segments (a
@@ -105,13 +106,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Bulk copy of `bytes` (multiple of 16) in pieces of at most 32 KB.
-__device__ __forceinline__ void fetch(uint8_t* dst, const void* src, uint32_t bytes, uint32_t bar) {
-  const uint8_t* s = static_cast<const uint8_t*>(src);
-  for (uint32_t o = 0; o < bytes; o += 32768u)
-    tc::bulk_load(smem_u32(dst + o), s + o, min(32768u, bytes - o), bar);
-}
-
 template <int M>
 __global__ void __launch_bounds__(kPsThreads, 1) proj_small_kernel(const SmallProjArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -125,27 +119,20 @@ __global__ void __launch_bounds__(kPsThreads, 1) proj_small_kernel(const SmallPr
   const int nrows = rhi - rlo;
   const PsLayout L = ps_layout(M, a.D, a.w_bytes, a.max_rows, absorb);
   const uint32_t rows_off = absorb && has_head ? kPsHeadBytes : 0u;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   const size_t row_bytes = (size_t)a.D * 2;
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // ---- this CTA's weights: independent of the previous kernel
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const uint32_t head_bytes = has_head ? kPsHeadBytes : 0u;
-    const uint32_t bytes = head_bytes + (uint32_t)(nrows * row_bytes);
-    tc::mbar_arrive_expect_tx(smem_u32(bar), bytes);
-    if (has_head)
-      fetch(smem, a.w_uk + (size_t)i * kNope * kLat, kPsHeadBytes, smem_u32(bar));
+  // ---- this CTA's weights (independent of the previous kernel)
+  {
+    if (has_head) cp_async_block(smem, a.w_uk + (size_t)i * kNope * kLat, kPsHeadBytes, tid, kPsThreads);
     // rows below 512 come from W^DKV, the others from W^KR
     const int d_hi = min(rhi, kLat), r_lo = max(rlo, kLat);
     if (d_hi > rlo)
-      fetch(smem + rows_off, a.w_dkv + (size_t)rlo * a.D, (uint32_t)((d_hi - rlo) * row_bytes),
-            smem_u32(bar));
+      cp_async_block(smem + rows_off, a.w_dkv + (size_t)rlo * a.D, (d_hi - rlo) * row_bytes, tid,
+                     kPsThreads);
     if (rhi > r_lo)
-      fetch(smem + rows_off + (size_t)(r_lo - rlo) * row_bytes, a.w_kr + (size_t)(r_lo - kLat) * a.D,
-            (uint32_t)((rhi - r_lo) * row_bytes), smem_u32(bar));
+      cp_async_block(smem + rows_off + (size_t)(r_lo - rlo) * row_bytes,
+                     a.w_kr + (size_t)(r_lo - kLat) * a.D, (rhi - r_lo) * row_bytes, tid, kPsThreads);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");   // h, q and seq_lens
 
@@ -161,8 +148,8 @@ __global__ void __launch_bounds__(kPsThreads, 1) proj_small_kernel(const SmallPr
     const int m = tid / kNope, r = tid % kNope;
     qs[tid] = __bfloat162float(a.q[((size_t)m * kHeads + i) * (kNope + kRope) + r]);
   }
+  cp_async_wait_all();
   __syncthreads();
-  if (!mbar_wait(bar, 0, a.status, 63)) return;
 
   float* red = reinterpret_cast<float*>(smem + L.off_red);    // [warp][M][512]
   float* part = reinterpret_cast<float*>(smem + L.off_part);  // [row][seg][M]
