@@ -695,7 +695,14 @@ bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsL
 bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int k_chunks,
                         const __nv_bfloat16* x, int M, int x_cols, __nv_bfloat16* out,
                         int ld_out, float* part, cudaStream_t st, const char* name) {
-  const GemmShape g = gemm_shape(ctx, M, m_tiles, k_chunks, 4, kSplitCap);
+  GemmShape g = gemm_shape(ctx, M, m_tiles, k_chunks, 4, kSplitCap);
+  if (k_chunks <= 8 && g.nt == 256) {
+    // many rows, short K (a prefill's up-projections): 128-token tiles, two
+    // CTAs per SM, no K split
+    g.nt = 128;
+    g.n_tiles = (M + 127) / 128;
+    g.splits = 1;
+  }
   if (g.n_tiles > 65535 || (g.splits > 1 && (long long)m_tiles * g.n_tiles > kCounters))
     return false;
   WgPlan p{};

@@ -30,11 +30,16 @@ namespace {
 // query launch at 256 tokens 72 -> 51 us).  Wide tiles of the long-K
 // projections keep one CTA per SM with a deep ring: halving the ring for two
 // CTAs per SM, with the extra K splits that brings, was measured slower
-// (W_O at 256 tokens 70 -> 82 us).
+// (W_O at 256 tokens 70 -> 82 us).  Row-major outputs with 128-token tiles
+// serve the short-K projections of a prefill (K^C and V of every cached row:
+// K = 512, eight chunks): three stages cover a tile's K and two CTAs share
+// an SM, so one CTA's epilogue overlaps the other's MMAs.
 template <int NT, int EPI = WG_ROWMAJOR> struct WgCfg {
+  static constexpr bool kShortK = EPI == WG_ROWMAJOR && NT == 128;
   static constexpr int kStages = EPI == WG_QIMG ? 2
+                               : kShortK ? 3
                                : NT == 16 ? 6 : NT == 32 ? 5 : NT == 64 ? 4 : NT == 128 ? 6 : 4;
-  static constexpr int kMinBlocks = (EPI == WG_QIMG || NT <= 64) ? 2 : 1;
+  static constexpr int kMinBlocks = (EPI == WG_QIMG || NT <= 64 || kShortK) ? 2 : 1;
   static constexpr uint32_t kA = 128 * 64 * 2;
   static constexpr uint32_t kB = NT * 64 * 2;
   static constexpr uint32_t kStage = kA + kB;
