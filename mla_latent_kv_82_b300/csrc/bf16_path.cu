@@ -201,11 +201,20 @@ struct GemmShape {
 };
 
 GemmShape gemm_shape(const mla_ctx* ctx, int M, int m_tiles, int k_chunks, int min_chunks,
-                     size_t partial_cap) {
+                     size_t partial_cap, bool rowmajor = false) {
   GemmShape g;
   g.nt = pick_token_tile(M, m_tiles);
+  if (rowmajor) {
+    // Row-major outputs run 128-token tiles in the short-K configuration
+    // (three stages, two CTAs per SM): K of at most eight chunks takes it
+    // at any width, longer K keeps 256-token tiles and their deep ring
+    if (k_chunks <= 8 && g.nt == 256) g.nt = 128;
+    if (k_chunks > 8 && g.nt == 128) g.nt = 256;
+  }
   g.n_tiles = (M + g.nt - 1) / g.nt;
-  g.splits = choose_k_splits(ctx, m_tiles, g.n_tiles, g.nt, k_chunks, partial_cap, min_chunks);
+  g.splits = rowmajor && g.nt == 128
+                 ? 1
+                 : choose_k_splits(ctx, m_tiles, g.n_tiles, g.nt, k_chunks, partial_cap, min_chunks);
   return g;
 }
 
@@ -221,12 +230,12 @@ Bf16Plans decode_plans(const mla_ctx* ctx, int M) {
   Bf16Plans p;
   p.abs = gemm_shape(ctx, M, kHeads * (kLat / 128), kNope / 64, 4, 0);
   p.abs.splits = 1;   // two K chunks only: never split
-  p.uv = gemm_shape(ctx, M, kHeads, kLat / 64, 4, kSplitCap);
-  p.o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap);
+  p.uv = gemm_shape(ctx, M, kHeads, kLat / 64, 4, kSplitCap, true);
+  p.o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap, true);
   if (dcq > 0) {
-    p.dq = gemm_shape(ctx, M, dcq / 128, D / 64, 4, kSplitCap);
-    p.uq = gemm_shape(ctx, M, kHeads, dcq / 64, 4, kSplitCap);
-    p.qr = gemm_shape(ctx, M, kHeads * kRope / 128, D / 64, 4, kSplitCap);
+    p.dq = gemm_shape(ctx, M, dcq / 128, D / 64, 4, kSplitCap, true);
+    p.uq = gemm_shape(ctx, M, kHeads, dcq / 64, 4, kSplitCap, true);
+    p.qr = gemm_shape(ctx, M, kHeads * kRope / 128, D / 64, 4, kSplitCap, true);
   }
   return p;
 }
@@ -695,14 +704,7 @@ bool bf16_query(mla_ctx* ctx, const __nv_bfloat16* h, int M, char* ws, const WsL
 bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int k_chunks,
                         const __nv_bfloat16* x, int M, int x_cols, __nv_bfloat16* out,
                         int ld_out, float* part, cudaStream_t st, const char* name) {
-  GemmShape g = gemm_shape(ctx, M, m_tiles, k_chunks, 4, kSplitCap);
-  if (k_chunks <= 8 && g.nt == 256) {
-    // many rows, short K (a prefill's up-projections): 128-token tiles, two
-    // CTAs per SM, no K split
-    g.nt = 128;
-    g.n_tiles = (M + 127) / 128;
-    g.splits = 1;
-  }
+  const GemmShape g = gemm_shape(ctx, M, m_tiles, k_chunks, 4, kSplitCap, true);
   if (g.n_tiles > 65535 || (g.splits > 1 && (long long)m_tiles * g.n_tiles > kCounters))
     return false;
   WgPlan p{};
@@ -732,8 +734,8 @@ bool bf16_rowmajor_gemm(mla_ctx* ctx, const CUtensorMap& wmap, int m_tiles, int 
 
 size_t prefill_partial_bytes(const mla_ctx* ctx, int R, int M) {
   const int D = ctx->cfg.d_model;
-  const GemmShape kv = gemm_shape(ctx, R, kHeads, kLat / 64, 4, kSplitCap);
-  const GemmShape o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap);
+  const GemmShape kv = gemm_shape(ctx, R, kHeads, kLat / 64, 4, kSplitCap, true);
+  const GemmShape o = gemm_shape(ctx, M, D / 128, kHeads * kDv / 64, 4, kSplitCap, true);
   return std::max(partial_bytes(kv, kHeads), partial_bytes(o, D / 128));
 }
 
