@@ -148,6 +148,29 @@ def test_bad_page_id_is_reported_not_written():
     assert st.mla.check_status() == 0      # the status word was cleared
 
 
+@pytest.mark.parametrize("lens,T", [([10], 1), ([10], 2), ([10, 70], 1), ([10, 20, 30], 1)])
+def test_bad_position_is_reported_not_written(lens, T):
+    """A new token whose position lies beyond max_position is reported and
+    its row is written nowhere; the other new tokens' rows are written (one
+    or two tokens run the CUDA-core projection kernel, three the GEMM)."""
+    wl = small_bf16(lens, T)
+    from mla_latent_kv_82_b300.workload import DeviceState
+    st = DeviceState(wl, sentinel=7.0)
+    before = st.cache.clone()
+    pos = st.pos_new.clone()
+    pos[0] = 10 ** 6
+    st.mla.compress_append(st.h_new, pos, st.bt, st.cache, wl.B, wl.T)
+    assert st.mla.check_status() == 6      # MLA_ERR_DEVICE_INDEX
+    P = wl.dims.page_size
+    changed = (st.cache != before).any(dim=1).nonzero().flatten().tolist()
+    allowed = set()
+    for m in range(1, wl.B * wl.T):
+        p_m = int(pos[m])
+        allowed.add(int(st.bt[m // wl.T, p_m // P]) * P + p_m % P)
+    assert set(changed) <= allowed and len(changed) == len(allowed)
+    assert st.mla.check_status() == 0
+
+
 @pytest.mark.parametrize("make", [
     lambda: tiny_f32([5, 40, 64], 1),
     lambda: small_bf16([0, 63, 200, 1000], 1),
