@@ -114,6 +114,8 @@ def _compare(st, seqs=None, exact_too=False):
     (2, [200]),
     (1, [70, 1]),
     (4, [3, 130, 260]),
+    (5, [63]),
+    (8, [0, 100]),      # the largest decode T
 ])
 def test_small_fp8(T, lens):
     _compare(_run(small_bf16(lens, T)), exact_too=True)

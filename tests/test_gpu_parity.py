@@ -65,6 +65,10 @@ def _compare_all(st, form="explicit", seqs=None, keep_rows=None):
     (1, [70, 1]),        # two tokens from two sequences
     (3, [2, 64, 190]),   # odd T > 1: single-CTA kernel, three tokens per split
     (4, [3, 130, 260]),  # T = 4: two CTA pairs per split
+    (5, [0, 70, 200]),   # odd T: five single-token clusters per split
+    (6, [1, 64]),
+    (7, [62, 129]),
+    (8, [0, 63, 300]),   # the largest decode T: four token pairs per split
 ])
 def test_small_bf16_explicit(T, lens):
     st = _run(small_bf16(lens, T))
@@ -78,7 +82,7 @@ def test_small_bf16_latent_output():
 
 @pytest.mark.parametrize("T,lens,page", [
     (1, [63], 64), (1, [0, 15, 16, 17, 100], 16), (2, [0, 14, 15, 33], 16), (1, [40, 3], 1),
-    (3, [0, 20, 47], 16)])
+    (3, [0, 20, 47], 16), (8, [0, 9, 40], 16)])
 def test_tiny_f32(T, lens, page):
     st = _run(tiny_f32(lens, T, page))
     _compare_all(st, "explicit")
@@ -203,6 +207,35 @@ def test_bad_length_is_reported():
     st.seq_lens.fill_(10 ** 6)             # beyond max_pages * page_size
     st.decode()
     assert st.mla.check_status() == 6
+
+
+@pytest.mark.parametrize("call", ["decode", "append_decode"])
+def test_more_than_eight_query_tokens_are_refused(call):
+    """T = 9 is refused before anything is enqueued; the output keeps its bytes."""
+    import mla_latent_kv_82_b300 as m
+    from mla_latent_kv_82_b300.workload import DeviceState
+    st = DeviceState(small_bf16([10], 1), prefill=False)
+    d, T = st.wl.dims, 9
+    q = torch.zeros((1, T, d.n_heads, d.d_nope + d.d_rope), dtype=torch.bfloat16, device=st.dev)
+    h = torch.zeros((1, T, d.d_model), dtype=torch.bfloat16, device=st.dev)
+    pos = torch.arange(T, dtype=torch.int32, device=st.dev)
+    seq_lens = torch.full((1,), T, dtype=torch.int32, device=st.dev)
+    out = torch.zeros((1, T, d.d_model), dtype=torch.bfloat16, device=st.dev)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=st.dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    before = st.mla.launch_count()
+    common = (st.cache.data_ptr(), st.num_pages, st.bt.data_ptr(), st.bt.shape[1],
+              seq_lens.data_ptr(), 1, T, out.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+    if call == "decode":
+        rc = m.mla_decode(st.mla.ctx, q.data_ptr(), *common)
+    else:
+        rc = m.mla_append_decode(st.mla.ctx, h.data_ptr(), pos.data_ptr(), q.data_ptr(), *common)
+    assert rc == m.MLA_ERR_INVALID_ARG
+    assert st.mla.launch_count() == before
+    torch.cuda.synchronize()
+    assert st.mla.check_status() == 0
+    assert not out.any()
 
 
 def test_bounded_wait_gives_up_with_status():

@@ -74,7 +74,7 @@ def _compare(st, form, seqs=None, heads_explicit=0):
 
 
 @pytest.mark.parametrize("T,lens", [(1, [0, 63, 200, 1000]), (2, [1, 64, 300]), (1, [77]),
-                                    (2, [130]), (1, [9, 200]), (3, [5, 130])])
+                                    (2, [130]), (1, [9, 200]), (3, [5, 130]), (8, [4, 70])])
 def test_layer_step_small_bf16(T, lens):
     _compare(_run(small_bf16(lens, T)), "explicit")
 
