@@ -172,6 +172,8 @@ size_t mla_decode_workspace_size(const mla_ctx* ctx, int batch, int T,
  *   out        device, [batch, T, d_model]: u = W_O [o_1 ... o_{n_h}].
  *   workspace  device scratch of at least mla_decode_workspace_size bytes,
  *              256-byte aligned; its contents need not be initialised.
+ * 1 <= T <= 8 (longer chunks go through mla_prefill): other T, a null or
+ * misaligned pointer return MLA_ERR_INVALID_ARG before anything is enqueued.
  * A length outside [T, max_pages*page_size] or a bad page id sets
  * MLA_ERR_DEVICE_INDEX on the device; the bad part is skipped. */
 mla_status mla_decode(mla_ctx* ctx, const void* q, const void* cache,
