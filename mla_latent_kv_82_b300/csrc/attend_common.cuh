@@ -76,17 +76,6 @@ __device__ __forceinline__ int nslabs_of(int tile_start, int p1) {
   return v >= kTile ? 4 : (v + 31) / 32;
 }
 
-// Pool row of token p of sequence sb (page id from the block table; a bad id
-// is reported and replaced by page 0 so that the TMA stays in bounds).
-__device__ __forceinline__ int page_row(const AttArgs& a, int sb, int p) {
-  int pg = a.bt[(size_t)sb * a.max_pages + p / kPage];
-  if (pg < 0 || pg >= a.num_pages) {
-    report(a.status, MLA_ERR_DEVICE_INDEX, 4000000 + sb);
-    pg = 0;
-  }
-  return pg * kPage;
-}
-
 // Block-table entries of a tile's two pages.  The producer loads them one
 // tile ahead of use and validates them only when used, so the global-load
 // latency stays off its per-stage issue path.
@@ -192,9 +181,6 @@ struct RingPos {
       s = 0;
       ph ^= 1u;
     }
-  }
-  __device__ __forceinline__ void skip(int m) {
-    for (int j = 0; j < m; ++j) next();
   }
 };
 

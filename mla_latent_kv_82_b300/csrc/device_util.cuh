@@ -173,12 +173,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
 // Global page range [g0, g1) of split c when P pages are cut into G splits.
 __device__ __forceinline__ void split_range(int c, long long P, int G, long long* g0,
                                             long long* g1) {

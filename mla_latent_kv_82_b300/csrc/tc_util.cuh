@@ -84,14 +84,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                   reinterpret_cast<uint64_t>(src)),
-               "r"(bytes)
-               : "memory");
-}
-
 // Make generic-proxy shared-memory writes visible to the async proxy (MMA, TMA).
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -204,19 +196,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 16 raw 32-bit words stored to the thread's lane row.
-__device__ __forceinline__ void tmem_st16_u32(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32"
-      " [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // 32 lanes x 64 consecutive 32-bit columns into each thread's 64 registers;
 // the wait is part of the same statement, so no use can be scheduled ahead
 // of it.
@@ -286,18 +265,11 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive (release at cluster scope) on an mbarrier given by its cluster
-// address.  The release makes this thread's earlier ordinary stores visible
-// to the other CTA; it costs over a thousand cycles.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
 // Relaxed arrive on a cluster mbarrier: for signalling an event that is
 // already complete by hardware rule (a copy whose completion this thread
 // observed, TMEM stores or loads it waited for), with no ordinary stores to
-// publish.  Costs a few hundred cycles less than the release form.
+// publish.  A release arrive at cluster scope (needed only to publish such
+// stores) costs over a thousand cycles; this one a few hundred fewer.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
@@ -323,30 +295,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z,
-                                            int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                                  int z, uint32_t even_bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(even_bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                                 int z, int w, uint32_t even_bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(w), "r"(even_bar)
       : "memory");
 }
 
@@ -401,16 +355,6 @@ __device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
-// Arrive once on the mbarrier at this shared offset in both CTAs of the pair
-// when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma2_commit_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- cluster data
 // Arrive once on the mbarrier at this shared offset in every CTA of the
 // cluster named in `mask` (bit r = cluster rank r) when every MMA this thread
@@ -429,25 +373,6 @@ __device__ __forceinline__ void mma2_commit_mc(uint32_t bar, uint16_t mask) {
       "[%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
-}
-
-// 16-byte and 4-byte stores into the shared memory of a CTA of the cluster
-// (cluster address from mapa_shared).
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                              uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a),
-               "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
-}
-
-// Order this thread's generic-proxy writes to shared memory anywhere in the
-// cluster before later async-proxy accesses (tensor-core operand reads).
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // 32 raw 32-bit words stored to the thread's lane row (32 columns), then
