@@ -6,6 +6,8 @@ named workloads run at full size with every sequence (tiny-fp32, b1-l4096)
 or a seeded sample of sequences (b64-paged, b128-l16k-t2, b4-l128k) compared
 with the oracle.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -73,6 +75,18 @@ def _compare_all(st, form="explicit", seqs=None, keep_rows=None):
 def test_small_bf16_explicit(T, lens):
     st = _run(small_bf16(lens, T))
     _compare_all(st, "explicit")
+
+
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_widest_model(T):
+    """d_model = 16384, the widest model the bf16 path takes (W_O 512 MB):
+    for one or two tokens the CUDA-core append kernel cannot hold its share
+    of [W^DKV; W^KR] rows in shared memory at this width, so the append and
+    absorbed query run on the tensor-core GEMM instead; W_O streams 32 KB
+    rows."""
+    wl = W.Workload(f"v2-d16384-T{T}", dataclasses.replace(W.V2, d_model=16384), "bf16",
+                    [3, 70], T, True)
+    _compare_all(_run(wl), "explicit")
 
 
 def test_small_bf16_latent_output():

@@ -6,6 +6,8 @@ in the explicit form (or the absorbed form on all heads at full size, with
 two heads per sampled sequence also in the explicit form); the CUDA path
 runs the query projections, the append and the decode through the C ABI.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -77,6 +79,13 @@ def _compare(st, form, seqs=None, heads_explicit=0):
                                     (2, [130]), (1, [9, 200]), (3, [5, 130]), (8, [4, 70])])
 def test_layer_step_small_bf16(T, lens):
     _compare(_run(small_bf16(lens, T)), "explicit")
+
+
+def test_layer_step_widest_model():
+    """The query path at d_model = 16384 (W^DQ and W^QR read 32 KB rows)."""
+    wl = W.Workload("v2-d16384-qp", dataclasses.replace(W.V2, d_model=16384), "bf16",
+                    [5, 66], 1, True)
+    _compare(_run(wl), "explicit")
 
 
 @pytest.mark.parametrize("T,lens", [(1, [63]), (2, [0, 30, 100])])
